@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE decode layer on B300 (one JSON line on rank 0).
+
+Default workload: full-width single MoE layer at batch 1 -- hidden 4096, 512
+experts, top-4 routed (softmax renormalised over the 4) + 1 shared expert,
+expert intermediate 1024, 4-bit codes with bf16 scale/bias per 64 inputs,
+bf16 router; 1000 decode tokens with x ~ N(0, 1).  One step = those 1000
+tokens, each one moe_layer_decode call at B = 1 (one fused kernel launch),
+replayed from a CUDA graph.  Inputs: 3.6 GB of routed experts (far larger than
+L2); the shared expert and the router (11 MB) are rotated over 16 copies so
+that consecutive tokens do not find them in L2, as in a model whose other
+layers evict them.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config 2|3|4|5] [--batch B]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FULL = dict(hidden=4096, inter=1024, n_experts=512, top_k=4)
+TOKENS = 1000
+COPIES = 16
+FALLBACK_HBM_GBS = 6400.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", type=int, default=2, choices=[2, 3, 4])
+    p.add_argument("--batch", type=int, default=1)
+    p.add_argument("--tokens", type=int, default=TOKENS)
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--experts", type=int, default=512, help="routed experts (smaller pools for profiling runs)")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:  # noqa: BLE001
+            self.proc.kill()
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("moe_fused.cu", "moe_device.cuh", "moe_kernels.cu"):
+        with open(os.path.join(ROOT, "bit_expert_matvec_moe_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{name}.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        if p.get("source_sha") == kernel_source_sha():
+            return p.get("dram_bytes_per_launch")
+    except Exception:  # noqa: BLE001
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- workload
+def build_full_layer(torch, M, bits=4, copies=COPIES, n_experts=512):
+    """Full-width layer on the device: 512 routed experts, `copies` copies of the
+    shared expert and router (identical bytes, distinct addresses)."""
+    from synth import device as SD
+    from synth import generate as G
+
+    d = M.Dims(bits=bits, flags=M.MOE_HAS_SHARED, **{**FULL, "n_experts": n_experts})
+    H, I, E = d.hidden, d.inter, d.n_experts
+    stride = M.moe_packed_expert_bytes(d, bits)
+    experts = torch.empty((E, stride), dtype=torch.uint8, device="cuda")
+
+    def pack(canon, b, dst):
+        M.moe_pack_weights(M.Dims(bits=b, flags=M.MOE_HAS_SHARED, **{**FULL, "n_experts": n_experts}), b,
+                           [canon[m][0] for m in ("gate", "up", "down")],
+                           [canon[m][1] for m in ("gate", "up", "down")],
+                           [canon[m][2] for m in ("gate", "up", "down")], dst)
+
+    for e in range(E):
+        pack(SD.expert(G.SEED, 0, e, H, I, bits), bits, experts[e])
+    sbytes = M.moe_packed_expert_bytes(d, 4)
+    shared = torch.empty((copies, sbytes), dtype=torch.uint8, device="cuda")
+    pack(SD.expert(G.SEED, 0, G.SHARED_EXPERT, H, I, 4), 4, shared[0])
+    router_np = G.router(G.SEED, 0, E, H)
+    router = torch.from_numpy(router_np.view(np.int16)).cuda().unsqueeze(0).repeat(copies, 1, 1).contiguous()
+    for c in range(1, copies):
+        shared[c].copy_(shared[0])
+    torch.cuda.synchronize()
+    return d, experts, stride, shared, router
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import bit_expert_matvec_moe_b300 as M
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    from synth import generate as G
+
+    bits = 2 if args.config == 4 else 4
+    d, experts, stride, shared, router = build_full_layer(torch, M, bits=bits, n_experts=args.experts)
+    B = args.batch
+    T = args.tokens
+    nsteps_tok = T // B
+    layers = [M.make_layer(d, experts, stride, router[c], shared=shared[c], shared_bits=4) for c in range(COPIES)]
+    h_host = G.hidden_states(G.SEED, 100 + rank, T, d.hidden)
+    h0 = torch.from_numpy(h_host).cuda()
+    h = h0.clone()
+    ws = torch.empty(M.moe_workspace_bytes(d, B), dtype=torch.uint8, device="cuda")
+    M.moe_workspace_init(ws)
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, d.top_k), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def one_step():
+        for t in range(nsteps_tok):
+            sl = slice(t * B, (t + 1) * B)
+            M.moe_layer_decode(layers[t % COPIES], h[sl], ws, idx_out=idx[sl], w_out=w[sl], stream=stream)
+
+    # correctness smoke of the configuration (status word) before timing
+    with torch.cuda.stream(stream):
+        one_step()
+    assert M.moe_get_device_status(ws, stream) == 0
+    graph = None
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                one_step()
+        except Exception as exc:  # noqa: BLE001
+            print(f"# CUDA graph capture failed ({exc}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
+    run = (lambda: graph.replay()) if graph is not None else one_step
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            h.copy_(h0)
+            run()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms = []
+    with torch.cuda.stream(stream):
+        # h is updated in place; resetting it (16 MB) is outside the event pair of each step
+        for _ in range(args.steps):
+            h.copy_(h0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            e1.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    assert M.moe_get_device_status(ws, stream) == 0
+    ms = float(np.mean(step_ms))
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # hidden states from pinned memory, the decode calls, D2H of the outputs
+    h_pin = torch.from_numpy(h_host).pin_memory()
+    y_pin = torch.empty_like(h_pin).pin_memory()
+    idx_pin = torch.empty((T, d.top_k), dtype=torch.int32).pin_memory()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for it in range(args.warmup + args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            h.copy_(h_pin, non_blocking=True)
+            run()
+            y_pin.copy_(h, non_blocking=True)
+            idx_pin.copy_(idx, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+    e2e = float(np.mean(e2e_ms))
+
+    expert_bytes = d.top_k * M.moe_packed_expert_bytes(d, bits) + M.moe_packed_expert_bytes(d, 4)
+    router_bytes = d.n_experts * d.hidden * 2
+    launches_per_step = nsteps_tok
+    per_launch_s = ms / 1e3 / launches_per_step
+    tok_s = T * world / (ms / 1e3)
+    peak, peak_kind = measured_hbm_peak()
+    alg = (expert_bytes + router_bytes) * B if B == 1 else None
+    achieved = (expert_bytes + router_bytes) / per_launch_s / 1e9 if B == 1 else None
+    out = {
+        "metric": "MoE layer decode tokens/s; expert-weight HBM GB/s vs ~8 TB/s peak",
+        "value": round(tok_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u4 codes x fp32 activations (int32 dp4a group sums, fp32 accumulate)" if bits == 4 else
+                 "u2 codes x fp32 activations (int32 dp4a group sums, fp32 accumulate)",
+        "data": "synthetic (seeded SplitMix64; random-init weights of the stated shape)",
+        "config": {
+            "workload": (f"full-width single MoE layer, batch {B}: hidden 4096, {d.n_experts} experts, top-4 routed + 1 shared, "
+                         f"inter 1024, {bits}-bit group-64 affine quant, bf16 router, {T} decode tokens"),
+            "batch": B, "tokens_per_step": T, "launches_per_step": launches_per_step,
+            "l2": f"inputs larger than L2 (3.6 GB routed experts); shared expert + router rotated over {COPIES} copies",
+            "graph": graph is not None, "parallelism": f"replicas x{world}",
+        },
+        "expert_gbs": round(expert_bytes * tok_s / world / 1e9, 1),
+        "us_per_token": round(ms * 1e3 / T, 3),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "fused_decode_kernel",
+            "achieved": round(achieved, 1) if achieved else None,
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4) if achieved else None,
+            "algorithmic_bytes_per_launch": alg,
+            "traffic": profiled_traffic("fused_decode_full_b1"),
+        },
+        "e2e": {"value": round(T * world / (e2e / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_pin.numel() * 4), "d2h_bytes_per_step": int(y_pin.numel() * 4 + idx_pin.numel() * 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": ck,
+    }
+    print(f"# {tok_s:.1f} tokens/s, {ms * 1e3 / T:.3f} us/token, e2e {e2e:.3f} ms/step", file=sys.stderr, flush=True)
+    if rank == 0 and args.config == 2 and B == 1 and args.cpu_seconds > 0:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) timing
+def cpu_baseline(seconds: float, tokens_max: int = 64):
+    """The fp64 oracle as it stands, one thread, on a bounded sample of the same
+    workload, run in a child process whose BLAS is pinned to one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", str(seconds),
+                          str(tokens_max)], capture_output=True, text=True, env=env, timeout=600)
+    if res.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + res.stderr[-2000:])
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def _cpu_baseline_child(seconds: float, tokens_max: int):
+    """Tokens are decoded one by one until `seconds` of oracle time pass.  The
+    touched experts are generated before each token's timing (input generation
+    is not oracle work)."""
+    from oracle import moe_oracle as O
+    from synth import generate as G
+
+    H, I, E, K = FULL["hidden"], FULL["inter"], FULL["n_experts"], FULL["top_k"]
+    R = G.router(G.SEED, 0, E, H)
+    h = G.hidden_states(G.SEED, 100, tokens_max, H)
+    shared = G.expert(G.SEED, 0, G.SHARED_EXPERT, H, I, 4)
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache[e] = G.expert(G.SEED, 0, e, H, I, 4)
+        return cache[e]
+
+    done, spent = 0, 0.0
+    while done < tokens_max and spent < seconds:
+        xn = O.rmsnorm(h[done], None, 1e-6)
+        for e in O.topk(O.router_logits(R, xn), K):
+            get(int(e))  # generation outside the timed region
+        t0 = time.perf_counter()
+        O.layer_decode(h[done], experts=get, shared=shared, router_bits=R, top_k=K, hidden=H, inter=I)
+        spent += time.perf_counter() - t0
+        done += 1
+    return {"value": round(done / spent, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of the {TOKENS} decode tokens of the same layer, fp64 numpy, 1 thread"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import time as _t
+
+    t_all = []
+    for it in range(args.warmup + args.steps):
+        cb = cpu_baseline(max(2.0, args.cpu_seconds / max(1, args.steps)), tokens_max=8)
+        if it >= args.warmup:
+            t_all.append(cb)
+    vals = [c["value"] for c in t_all]
+    v = float(np.mean(vals))
+    out = {
+        "impl": "reference",
+        "metric": "MoE layer decode tokens/s; expert-weight HBM GB/s vs ~8 TB/s peak",
+        "value": round(v, 3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 / v, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64; random-init weights of the stated shape)",
+        "config": {"workload": ("full-width single MoE layer, batch 1: hidden 4096, 512 experts, top-4 routed + 1 "
+                                "shared, inter 1024, 4-bit group-64 affine quant, bf16 router; each step a bounded "
+                                "sample of its decode tokens"), "parallelism": "host cores, 1 thread"},
+        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": t_all[-1]["sample"]},
+        "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    _t.sleep(0)
+
+
+def main():
+    if len(sys.argv) == 4 and sys.argv[1] == "--cpu-baseline-child":
+        print(json.dumps(_cpu_baseline_child(float(sys.argv[2]), int(sys.argv[3]))))
+        return
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,466 @@
+// C ABI of the MoE decode path: argument checks, workspace layout and launches.
+// Declarations and their contract: include/moe.h.
+#include <cmath>
+#include <cstring>
+#include <string>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status cuda_fail(cudaError_t e) {
+  g_last_error = cudaGetErrorString(e);
+  return MOE_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dims_ok(const moe_dims* d) {
+  if (!d) return false;
+  if (d->group != MOE_GROUP) return false;
+  if (d->hidden <= 0 || d->hidden % MOE_GROUP || d->hidden > MOE_MAX_HIDDEN) return false;
+  if (d->inter <= 0 || d->inter % MOE_GROUP || d->inter > MOE_MAX_INTER) return false;
+  if (d->n_experts < 1 || d->n_experts > MOE_MAX_EXPERTS) return false;
+  if (d->top_k < 1 || d->top_k > MOE_MAX_TOPK || d->top_k > d->n_experts) return false;
+  if (d->bits != 4 && d->bits != 2) return false;
+  if (!(d->rms_eps >= 0.f) || !std::isfinite(d->rms_eps)) return false;
+  if (d->flags & ~(MOE_HAS_SHARED | MOE_HAS_SHARED_GATE | MOE_NO_FUSED)) return false;
+  if ((d->flags & MOE_HAS_SHARED_GATE) && !(d->flags & MOE_HAS_SHARED)) return false;
+  return true;
+}
+
+struct WsLayout {
+  size_t logits, idx, w, gs, xn, xq4, xe4, xq2, xe2, a, aq4, ae4, aq2, ae2, d, nuniq, uniq_e, uniq_off, ent, total;
+};
+
+// Byte offsets of the workspace regions for a batch of B tokens.  Only the
+// 256-byte header (status word, barrier counters) lives across calls.
+WsLayout ws_layout(const moe_dims& d, int B) {
+  WsLayout L{};
+  size_t o = sizeof(WsHeader);
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = (o + bytes + 255) & ~size_t(255);
+    return at;
+  };
+  const size_t E = d.n_experts, K = d.top_k, H = d.hidden, I = d.inter;
+  const size_t ns = K + 1;  // routed slots plus the shared slot
+  const size_t ngh = H / MOE_GROUP, ngi = I / MOE_GROUP;
+  L.logits = take(B * (E + 1) * 4);
+  L.idx = take(B * K * 4);
+  L.w = take(B * K * 4);
+  L.gs = take(B * 4);
+  L.xn = take(B * H * 4);
+  L.xq4 = take(B * ngh * kLimbWords * 4);
+  L.xe4 = take(B * ngh * 8);
+  L.xq2 = take(B * ngh * kLimbWords * 4);
+  L.xe2 = take(B * ngh * 8);
+  L.a = take(B * ns * I * 4);
+  L.aq4 = take(B * ns * ngi * kLimbWords * 4);
+  L.ae4 = take(B * ns * ngi * 8);
+  L.aq2 = take(B * ns * ngi * kLimbWords * 4);
+  L.ae2 = take(B * ns * ngi * 8);
+  L.d = take(B * ns * H * 4);
+  L.nuniq = take(4);
+  L.uniq_e = take((E + 1) * 4);
+  L.uniq_off = take((E + 2) * 4);
+  L.ent = take(B * ns * 4);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_packed_expert_bytes(const moe_dims* dims, int32_t bits) {
+  if (!dims_ok(dims) || (bits != 4 && bits != 2)) return 0;
+  return make_fmt(bits, dims->hidden, dims->inter).total;
+}
+
+size_t moe_workspace_bytes(const moe_dims* dims, int32_t max_batch) {
+  if (!dims_ok(dims) || max_batch < 1 || max_batch > MOE_MAX_BATCH) return 0;
+  return ws_layout(*dims, max_batch).total;
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || !aligned16(ws) || ws_bytes < sizeof(WsHeader)) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status moe_pack_weights(const moe_dims* dims, int32_t bits, const uint8_t* const codes[3],
+                            const uint16_t* const scales[3], const uint16_t* const biases[3], void* dst,
+                            moe_stream_t stream) {
+  if (!dims_ok(dims) || (bits != 4 && bits != 2) || !codes || !scales || !biases || !dst || !aligned16(dst))
+    return MOE_ERR_INVALID_ARG;
+  PackArgs a{};
+  a.f = make_fmt(bits, dims->hidden, dims->inter);
+  for (int m = 0; m < 3; ++m) {
+    if (!codes[m] || !scales[m] || !biases[m]) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(codes[m]) || (reinterpret_cast<uintptr_t>(scales[m]) & 1u) ||
+        (reinterpret_cast<uintptr_t>(biases[m]) & 1u))
+      return MOE_ERR_INVALID_ARG;
+    a.codes[m] = codes[m];
+    a.scales[m] = scales[m];
+    a.biases[m] = biases[m];
+  }
+  a.dst = static_cast<uint8_t*>(dst);
+  cudaError_t e = launch_pack(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status moe_route(const moe_dims* dims, const float* xn, int32_t B, const uint16_t* router,
+                     const float* logit_offset, int32_t* idx, float* w, float* logits_out, void* ws, size_t ws_bytes,
+                     moe_stream_t stream) {
+  if (!dims_ok(dims) || B < 1 || B > MOE_MAX_BATCH) return MOE_ERR_INVALID_ARG;
+  if (!xn || !router || !idx || !w || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xn) || !aligned16(router) || !aligned16(ws) || !aligned16(idx) || !aligned16(w) ||
+      (logit_offset && !aligned16(logit_offset)) || (logits_out && !aligned16(logits_out)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*dims, B);
+  if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  RouterArgs r{};
+  r.xn = xn;
+  r.B = B;
+  r.H = dims->hidden;
+  r.E = dims->n_experts;
+  r.router = router;
+  r.gate = nullptr;
+  r.offset = logit_offset;
+  r.logits = at<float>(ws, L.logits);
+  cudaError_t e = launch_router(r, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  TopkArgs t{};
+  t.logits = r.logits;
+  t.E = dims->n_experts;
+  t.K = dims->top_k;
+  t.has_gate = 0;
+  t.idx = idx;
+  t.w = w;
+  t.gs = nullptr;
+  t.logits_out = logits_out;
+  t.hdr = at<WsHeader>(ws, 0);
+  e = launch_topk(t, B, s);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* blob, const float* xn, int32_t B,
+                              const float* row_w, float* out, int32_t accumulate, void* ws, size_t ws_bytes,
+                              moe_stream_t stream) {
+  if (!dims_ok(dims) || (bits != 4 && bits != 2) || B < 1 || B > MOE_MAX_BATCH) return MOE_ERR_INVALID_ARG;
+  if (!blob || !xn || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(blob) || !aligned16(xn) || !aligned16(out) || !aligned16(ws) || (row_w && !aligned16(row_w)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*dims, B);
+  if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int H = dims->hidden, I = dims->inter;
+  WsHeader* hdr = at<WsHeader>(ws, 0);
+  const int lay = bits == 4 ? 1 : 2;
+
+  NormQuantArgs nq{};
+  nq.in = xn;
+  nq.n = H;
+  nq.do_norm = 0;
+  nq.layouts = lay;
+  nq.q4 = at<uint32_t>(ws, L.xq4);
+  nq.e4 = at<float2>(ws, L.xe4);
+  nq.q2 = at<uint32_t>(ws, L.xq2);
+  nq.e2 = at<float2>(ws, L.xe2);
+  nq.hdr = hdr;
+  cudaError_t e = launch_norm_quant(nq, B, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  GateUpArgs g{};
+  g.H = H;
+  g.I = I;
+  g.K = 0;
+  g.B = B;
+  g.nslots = 1;
+  g.bits = bits;
+  g.shared_bits = bits;
+  g.blob = static_cast<const uint8_t*>(blob);
+  g.xq4 = nq.q4;
+  g.xe4 = nq.e4;
+  g.xq2 = nq.q2;
+  g.xe2 = nq.e2;
+  g.a_out = at<float>(ws, L.a);
+  e = launch_gateup(g, 1, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  NormQuantArgs aq = nq;
+  aq.in = g.a_out;
+  aq.n = I;
+  aq.q4 = at<uint32_t>(ws, L.aq4);
+  aq.e4 = at<float2>(ws, L.ae4);
+  aq.q2 = at<uint32_t>(ws, L.aq2);
+  aq.e2 = at<float2>(ws, L.ae2);
+  e = launch_norm_quant(aq, B, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  DownArgs dn{};
+  dn.H = H;
+  dn.I = I;
+  dn.K = 0;
+  dn.B = B;
+  dn.nslots = 1;
+  dn.bits = bits;
+  dn.shared_bits = bits;
+  dn.blob = g.blob;
+  dn.aq4 = aq.q4;
+  dn.ae4 = aq.e4;
+  dn.aq2 = aq.q2;
+  dn.ae2 = aq.e2;
+  dn.d_out = at<float>(ws, L.d);
+  e = launch_down(dn, 1, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  CombineArgs cb{};
+  cb.B = B;
+  cb.H = H;
+  cb.K = 0;
+  cb.nslots = 1;
+  cb.single = 1;
+  cb.accumulate = accumulate ? 1 : 0;
+  cb.d = dn.d_out;
+  cb.row_w = row_w;
+  cb.out = out;
+  e = launch_combine(cb, s);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const float* logit_offset, int32_t* idx_out,
+                            float* w_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!layer || !dims_ok(&layer->d) || B < 1 || B > MOE_MAX_BATCH) return MOE_ERR_INVALID_ARG;
+  const moe_dims& d = layer->d;
+  const int has_shared = (d.flags & MOE_HAS_SHARED) ? 1 : 0;
+  const int has_gate = (d.flags & MOE_HAS_SHARED_GATE) ? 1 : 0;
+  if (!h || !ws || !layer->experts || !layer->router) return MOE_ERR_INVALID_ARG;
+  if (has_shared && (!layer->shared || (layer->shared_bits != 4 && layer->shared_bits != 2))) return MOE_ERR_INVALID_ARG;
+  if (has_gate && !layer->shared_gate) return MOE_ERR_INVALID_ARG;
+  const size_t blob = make_fmt(d.bits, d.hidden, d.inter).total;
+  if (layer->expert_stride < blob || layer->expert_stride % 16) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(ws) || !aligned16(layer->experts) || !aligned16(layer->router) ||
+      (has_shared && !aligned16(layer->shared)) || (layer->rms_gamma && !aligned16(layer->rms_gamma)) ||
+      (has_gate && !aligned16(layer->shared_gate)) || (logit_offset && !aligned16(logit_offset)) ||
+      (idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d, B);
+  if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = at<WsHeader>(ws, 0);
+  const int shared_bits = has_shared ? layer->shared_bits : d.bits;
+  cudaError_t e;
+
+  if (B == 1 && !(d.flags & MOE_NO_FUSED)) {
+    FusedPlan plan;
+    if (fused_plan(d.hidden, d.inter, d.n_experts, d.top_k, d.bits, shared_bits, has_shared, current_device(), &plan)) {
+      FusedArgs f{};
+      f.H = d.hidden;
+      f.I = d.inter;
+      f.E = d.n_experts;
+      f.K = d.top_k;
+      f.bits = d.bits;
+      f.shared_bits = shared_bits;
+      f.has_shared = has_shared;
+      f.has_gate = has_gate;
+      f.eps = d.rms_eps;
+      f.experts = static_cast<const uint8_t*>(layer->experts);
+      f.stride = layer->expert_stride;
+      f.shared = static_cast<const uint8_t*>(layer->shared);
+      f.router = layer->router;
+      f.gamma = layer->rms_gamma;
+      f.gate = layer->shared_gate;
+      f.h = h;
+      f.offset = logit_offset;
+      f.idx_out = idx_out;
+      f.w_out = w_out;
+      f.hdr = hdr;
+      f.a_glob = at<float>(ws, L.a);
+      f.logits = at<float>(ws, L.logits);
+      f.plan = plan;
+      e = launch_fused(f, s);
+      return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+    }
+  }
+
+  // multi-kernel path
+  const int K = d.top_k, E = d.n_experts, H = d.hidden, I = d.inter;
+  const int nslots = K + has_shared;
+  const int lay = ((d.bits == 4 || shared_bits == 4) ? 1 : 0) | ((d.bits == 2 || shared_bits == 2) ? 2 : 0);
+  NormQuantArgs nq{};
+  nq.in = h;
+  nq.n = H;
+  nq.do_norm = 1;
+  nq.eps = d.rms_eps;
+  nq.gamma = layer->rms_gamma;
+  nq.xn_out = at<float>(ws, L.xn);
+  nq.layouts = lay;
+  nq.q4 = at<uint32_t>(ws, L.xq4);
+  nq.e4 = at<float2>(ws, L.xe4);
+  nq.q2 = at<uint32_t>(ws, L.xq2);
+  nq.e2 = at<float2>(ws, L.xe2);
+  nq.hdr = hdr;
+  if ((e = launch_norm_quant(nq, B, s)) != cudaSuccess) return cuda_fail(e);
+
+  RouterArgs r{};
+  r.xn = nq.xn_out;
+  r.B = B;
+  r.H = H;
+  r.E = E;
+  r.router = layer->router;
+  r.gate = has_gate ? layer->shared_gate : nullptr;
+  r.offset = logit_offset;
+  r.logits = at<float>(ws, L.logits);
+  if ((e = launch_router(r, s)) != cudaSuccess) return cuda_fail(e);
+
+  TopkArgs t{};
+  t.logits = r.logits;
+  t.E = E;
+  t.K = K;
+  t.has_gate = has_gate;
+  t.idx = at<int32_t>(ws, L.idx);
+  t.w = at<float>(ws, L.w);
+  t.gs = at<float>(ws, L.gs);
+  t.idx_out = idx_out;
+  t.w_out = w_out;
+  t.hdr = hdr;
+  if ((e = launch_topk(t, B, s)) != cudaSuccess) return cuda_fail(e);
+
+  BucketArgs bk{};
+  bk.idx = t.idx;
+  bk.B = B;
+  bk.K = K;
+  bk.E = E;
+  bk.has_shared = has_shared;
+  bk.nslots = nslots;
+  bk.n_uniq = at<int>(ws, L.nuniq);
+  bk.uniq_e = at<int>(ws, L.uniq_e);
+  bk.uniq_off = at<int>(ws, L.uniq_off);
+  bk.ent = at<int>(ws, L.ent);
+  if ((e = launch_bucket(bk, s)) != cudaSuccess) return cuda_fail(e);
+  const int items = std::min(B * K, E) + has_shared;
+
+  GateUpArgs g{};
+  g.H = H;
+  g.I = I;
+  g.K = K;
+  g.B = B;
+  g.nslots = nslots;
+  g.bits = d.bits;
+  g.shared_bits = shared_bits;
+  g.experts = static_cast<const uint8_t*>(layer->experts);
+  g.stride = layer->expert_stride;
+  g.shared = static_cast<const uint8_t*>(layer->shared);
+  g.n_uniq = bk.n_uniq;
+  g.uniq_e = bk.uniq_e;
+  g.uniq_off = bk.uniq_off;
+  g.ent = bk.ent;
+  g.xq4 = nq.q4;
+  g.xe4 = nq.e4;
+  g.xq2 = nq.q2;
+  g.xe2 = nq.e2;
+  g.a_out = at<float>(ws, L.a);
+  if ((e = launch_gateup(g, items, s)) != cudaSuccess) return cuda_fail(e);
+
+  NormQuantArgs aq{};
+  aq.in = g.a_out;
+  aq.n = I;
+  aq.do_norm = 0;
+  aq.layouts = lay;
+  aq.q4 = at<uint32_t>(ws, L.aq4);
+  aq.e4 = at<float2>(ws, L.ae4);
+  aq.q2 = at<uint32_t>(ws, L.aq2);
+  aq.e2 = at<float2>(ws, L.ae2);
+  aq.hdr = hdr;
+  if ((e = launch_norm_quant(aq, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
+
+  DownArgs dn{};
+  dn.H = H;
+  dn.I = I;
+  dn.K = K;
+  dn.B = B;
+  dn.nslots = nslots;
+  dn.bits = d.bits;
+  dn.shared_bits = shared_bits;
+  dn.experts = g.experts;
+  dn.stride = g.stride;
+  dn.shared = g.shared;
+  dn.n_uniq = bk.n_uniq;
+  dn.uniq_e = bk.uniq_e;
+  dn.uniq_off = bk.uniq_off;
+  dn.ent = bk.ent;
+  dn.aq4 = aq.q4;
+  dn.ae4 = aq.e4;
+  dn.aq2 = aq.q2;
+  dn.ae2 = aq.e2;
+  dn.d_out = at<float>(ws, L.d);
+  if ((e = launch_down(dn, items, s)) != cudaSuccess) return cuda_fail(e);
+
+  CombineArgs cb{};
+  cb.B = B;
+  cb.H = H;
+  cb.K = K;
+  cb.nslots = nslots;
+  cb.has_shared = has_shared;
+  cb.single = 0;
+  cb.d = dn.d_out;
+  cb.w = t.w;
+  cb.gs = t.gs;
+  cb.out = h;
+  if ((e = launch_combine(cb, s)) != cudaSuccess) return cuda_fail(e);
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(void* ws, moe_stream_t stream) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  WsHeader hh;
+  e = cudaMemcpy(&hh, ws, sizeof(hh), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (hh.status || hh.abort) {
+    e = cudaMemset(ws, 0, sizeof(WsHeader));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (hh.status & ST_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (hh.status & ST_NONFINITE) return MOE_ERR_NONFINITE;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_NONFINITE: return "non-finite activation";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error_message(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

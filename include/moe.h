@@ -1,0 +1,208 @@
+/*
+ * moe.h - C ABI of the B300 (sm_103a) decode-time Mixture-of-Experts expert path.
+ *
+ * One token (or a small batch of tokens) through one MoE layer: RMSNorm, a
+ * bf16 router matvec, softmax and top-K over the experts, for each chosen
+ * expert a fused affine-dequantised (4-bit or 2-bit codes, per-group bf16
+ * scale and bias) gate/up matvec with SwiGLU and a dequantised down matvec,
+ * then the routing-weighted combine with an always-on shared expert and the
+ * residual.  The Flash-MoE pages describe this path for Apple GPUs:
+ *   - "397B MoE sur MacBook : 4,4 t/s Moteur Flash-MoE", "Techniques de
+ *     rupture" items 1-4 (K active experts per layer, FMA-rewritten
+ *     nibble*scale+bias dequant, fused SwiGLU, RMS norm, MoE combine);
+ *   - "Flash-MoE - Dizüstünde 397 milyar parametreli modeli çalıştırma",
+ *     "Model mimarisi" (512 experts, hidden 4096) and "Metal Compute
+ *     Shaders" (MoE combine + residual + gate).
+ *
+ * Conventions for every entry point
+ *   - All pointers named "device" are CUDA device pointers owned by the caller;
+ *     the library never allocates, frees or keeps them.  Every device pointer
+ *     must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *     stream.  Work is enqueued asynchronously; no call synchronises except
+ *     moe_get_device_status.
+ *   - Host-detectable errors (bad sizes, NULL or misaligned pointers, a
+ *     workspace that is too small) return at once, before anything is
+ *     enqueued.  A failed launch returns MOE_ERR_CUDA (moe_last_error_message()
+ *     gives the CUDA error text).  Errors found on the device (a bounded wait
+ *     that ran out, a non-finite activation) are recorded in the workspace
+ *     status word and read with moe_get_device_status.
+ *   - Calls that share a workspace must be ordered on one stream; calls on
+ *     different streams need different workspaces.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* moe_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* a size, pointer, alignment or flag is not valid */
+  MOE_ERR_UNSUPPORTED = 2, /* valid, but outside what the kernels implement */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 4,     /* a device-side wait ran out of time (status word) */
+  MOE_ERR_NONFINITE = 5    /* a non-finite activation was seen (status word) */
+} moe_status;
+
+/* flags of moe_dims */
+#define MOE_HAS_SHARED 1      /* the layer has one always-on shared expert */
+#define MOE_HAS_SHARED_GATE 2 /* the shared expert is scaled by sigmoid(shared_gate . xn) */
+#define MOE_NO_FUSED 4        /* moe_layer_decode: take the multi-kernel path even for B == 1 */
+
+/* Limits of this implementation (checked on entry). */
+#define MOE_MAX_TOPK 8
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_HIDDEN 8192
+#define MOE_MAX_INTER 4096
+#define MOE_MAX_BATCH 256
+#define MOE_GROUP 64
+
+/*
+ * Layer shape.  hidden H and inter I are multiples of `group`, which must be
+ * 64 (the scale/bias group along each matrix's input dimension).  `bits` is
+ * the code width of the routed experts, 4 or 2.  rms_eps is the RMSNorm
+ * epsilon (1e-6 in the workloads here).
+ */
+typedef struct {
+  int32_t hidden;
+  int32_t inter;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t bits;
+  int32_t group;
+  float rms_eps;
+  int32_t flags;
+} moe_dims;
+
+/*
+ * One MoE layer, all device pointers.
+ *   experts       n_experts packed blobs (moe_pack_weights), blob e at
+ *                 experts + e * expert_stride; expert_stride >= the packed
+ *                 size for dims.bits and a multiple of 16.
+ *   shared        packed blob of the shared expert (code width shared_bits,
+ *                 4 or 2), or NULL when MOE_HAS_SHARED is not set.
+ *   router        bf16 [n_experts, hidden], row-major.
+ *   rms_gamma     bf16 [hidden] or NULL (gamma = 1).
+ *   shared_gate   bf16 [hidden], read only when MOE_HAS_SHARED_GATE is set.
+ */
+typedef struct {
+  moe_dims d;
+  const void* experts;
+  size_t expert_stride;
+  const void* shared;
+  int32_t shared_bits;
+  const uint16_t* router;
+  const uint16_t* rms_gamma;
+  const uint16_t* shared_gate;
+} moe_layer;
+
+/*
+ * Bytes of one packed expert blob of the given code width.  Gate and up rows
+ * (inter rows of `hidden` inputs) and down rows (hidden rows of `inter`
+ * inputs) each hold their codes followed by one (bf16 scale, bf16 bias) pair
+ * per group; a row is padded to 16 bytes.  At hidden 4096, inter 1024, 4-bit
+ * this is 7,077,888 bytes: the pages' "~6.75 MB" per expert ("Techniques de
+ * rupture" item 1).  Returns 0 for invalid dims or bits.
+ */
+size_t moe_packed_expert_bytes(const moe_dims* dims, int32_t bits);
+
+/*
+ * Bytes of device workspace the calls below need for batches of up to
+ * max_batch tokens.  The workspace holds the device status word, the barrier
+ * counters of the single-token fused kernel and intermediate activations.
+ * Returns 0 for invalid arguments.
+ */
+size_t moe_workspace_bytes(const moe_dims* dims, int32_t max_batch);
+
+/*
+ * Zero a workspace (cudaMemsetAsync on `stream`).  Required once before the
+ * first use of a workspace; afterwards the kernels keep it consistent.
+ */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Repack one expert from the canonical layout into the blob the kernels read.
+ * Canonical input, per matrix m in (gate [inter, hidden], up [inter, hidden],
+ * down [hidden, inter]):
+ *   codes[m]   uint8 [rows, cols*bits/8], row-major; element c of a row is
+ *              bit field (c mod 8/bits) of byte c*bits/8, counted from the
+ *              least significant bit (low nibble = even element);
+ *   scales[m]  bf16 [rows, cols/64];  biases[m] bf16 [rows, cols/64];
+ *   weight     W[r][c] = code * scale[r][c/64] + bias[r][c/64]
+ *              ("nibble * scale + bias", "Techniques de rupture" item 2).
+ * dst receives moe_packed_expert_bytes(dims, bits) bytes.  Device pointers;
+ * code rows must start 16-byte aligned (cols*bits/8 a multiple of 16).
+ */
+moe_status moe_pack_weights(const moe_dims* dims, int32_t bits,
+                            const uint8_t* const codes[3],
+                            const uint16_t* const scales[3],
+                            const uint16_t* const biases[3],
+                            void* dst, moe_stream_t stream);
+
+/*
+ * Routing of B tokens (device pointers):
+ *   logits[b][e] = router[e] . xn[b] (+ logit_offset[b][e])  (fp32 accumulate)
+ *   idx[b][0..K)  the K experts with the largest logits, by (logit desc,
+ *                 index asc);  w[b][k] = softmax(logits[b])[idx] renormalised
+ *                 over the K chosen (so the weights of a token sum to 1).
+ * xn fp32 [B, hidden] is the normalised hidden state; logit_offset fp32
+ * [B, n_experts] or NULL; idx int32 [B, K]; w fp32 [B, K]; logits_out fp32
+ * [B, n_experts] or NULL.  The pages route on the CPU ("Pipeline GPU
+ * différé": "CPU : routage"); here routing stays on the device.
+ */
+moe_status moe_route(const moe_dims* dims, const float* xn, int32_t B,
+                     const uint16_t* router, const float* logit_offset,
+                     int32_t* idx, float* w, float* logits_out,
+                     void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * One expert on B tokens (device pointers):
+ *   g = Wg xn, u = Wu xn, a = silu(g) * u, d = Wd a   (SwiGLU expert)
+ *   out[b] = (accumulate ? out[b] : 0) + row_w[b] * d[b]
+ * blob is a packed expert of code width `bits`; xn fp32 [B, hidden]; row_w
+ * fp32 [B] or NULL (weight 1); out fp32 [B, hidden].
+ */
+moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* blob,
+                              const float* xn, int32_t B, const float* row_w,
+                              float* out, int32_t accumulate,
+                              void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * The whole layer on B tokens, in place on h (fp32 [B, hidden], device):
+ *   xn = RMSNorm(h) * gamma;  route(xn) -> idx, w;
+ *   h  = h + sum_k w_k * expert_{idx_k}(xn) + g_s * shared(xn)
+ * with g_s = 1, or sigmoid(shared_gate . xn) under MOE_HAS_SHARED_GATE.
+ * logit_offset fp32 [B, n_experts] or NULL is added to the router logits.
+ * idx_out int32 [B, K] and w_out fp32 [B, K] receive the routing, or NULL.
+ * B == 1 runs one cooperative persistent kernel; B > 1 groups the tokens by
+ * expert so that each touched expert is streamed once per call.
+ */
+moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B,
+                            const float* logit_offset, int32_t* idx_out, float* w_out,
+                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Synchronise `stream`, read the workspace status word, clear it and return
+ * it (MOE_OK when no device-side error was recorded).  After a device-side
+ * error the kernels of later calls return early until the status is cleared.
+ */
+moe_status moe_get_device_status(void* ws, moe_stream_t stream);
+
+/* Static text of a status code. */
+const char* moe_status_string(moe_status s);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if none). */
+const char* moe_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */
