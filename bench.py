@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--experts", type=int, default=512, help="routed experts (smaller pools for profiling runs)")
+    p.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch between decode calls")
     return p.parse_args()
 
 
@@ -115,7 +116,7 @@ class ClockSampler:
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("moe_fused.cu", "moe_device.cuh", "moe_kernels.cu"):
+    for f in ("moe_decode_b1.cu", "moe_device.cuh", "moe_kernels.cu"):
         with open(os.path.join(ROOT, "bit_expert_matvec_moe_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -180,6 +181,8 @@ def run_ours(args, rank, world, local):
 
     bits = 2 if args.config == 4 else 4
     d, experts, stride, shared, router = build_full_layer(torch, M, bits=bits, n_experts=args.experts)
+    if args.pdl:
+        d.flags |= M.MOE_PDL
     B = args.batch
     T = args.tokens
     nsteps_tok = T // B
@@ -298,7 +301,7 @@ def run_ours(args, rank, world, local):
         "us_per_token": round(ms * 1e3 / T, 3),
         "roofline": {
             "bound": "hbm",
-            "kernel": "fused_decode_kernel",
+            "kernel": "decode_b1_kernel",
             "achieved": round(achieved, 1) if achieved else None,
             "peak": peak,
             "peak_kind": peak_kind,

@@ -17,6 +17,7 @@ MOE_ERR_NONFINITE = 5
 MOE_HAS_SHARED = 1
 MOE_HAS_SHARED_GATE = 2
 MOE_NO_FUSED = 4
+MOE_PDL = 8
 
 # every symbol include/moe.h declares
 EXPORTS = (

@@ -29,20 +29,20 @@ bool dims_ok(const moe_dims* d) {
   if (d->top_k < 1 || d->top_k > MOE_MAX_TOPK || d->top_k > d->n_experts) return false;
   if (d->bits != 4 && d->bits != 2) return false;
   if (!(d->rms_eps >= 0.f) || !std::isfinite(d->rms_eps)) return false;
-  if (d->flags & ~(MOE_HAS_SHARED | MOE_HAS_SHARED_GATE | MOE_NO_FUSED)) return false;
+  if (d->flags & ~(MOE_HAS_SHARED | MOE_HAS_SHARED_GATE | MOE_NO_FUSED | MOE_PDL)) return false;
   if ((d->flags & MOE_HAS_SHARED_GATE) && !(d->flags & MOE_HAS_SHARED)) return false;
   return true;
 }
 
 struct WsLayout {
-  size_t logits, idx, w, gs, xn, xq4, xe4, xq2, xe2, a, aq4, ae4, aq2, ae2, d, nuniq, uniq_e, uniq_off, ent, total;
+  size_t logits, idx, w, gs, xn, xq, xe, a, aq, ae, d, nuniq, uniq_e, uniq_off, ent, pub_logits, pub_act, total;
 };
 
 // Byte offsets of the workspace regions for a batch of B tokens.  Only the
 // 256-byte header (status word, barrier counters) lives across calls.
 WsLayout ws_layout(const moe_dims& d, int B) {
   WsLayout L{};
-  size_t o = sizeof(WsHeader);
+  size_t o = kHeaderBytes;
   auto take = [&](size_t bytes) {
     const size_t at = o;
     o = (o + bytes + 255) & ~size_t(255);
@@ -56,20 +56,19 @@ WsLayout ws_layout(const moe_dims& d, int B) {
   L.w = take(B * K * 4);
   L.gs = take(B * 4);
   L.xn = take(B * H * 4);
-  L.xq4 = take(B * ngh * kLimbWords * 4);
-  L.xe4 = take(B * ngh * 8);
-  L.xq2 = take(B * ngh * kLimbWords * 4);
-  L.xe2 = take(B * ngh * 8);
+  L.xq = take(B * ngh * kLimbBytes);
+  L.xe = take(B * ngh * 8);
   L.a = take(B * ns * I * 4);
-  L.aq4 = take(B * ns * ngi * kLimbWords * 4);
-  L.ae4 = take(B * ns * ngi * 8);
-  L.aq2 = take(B * ns * ngi * kLimbWords * 4);
-  L.ae2 = take(B * ns * ngi * 8);
+  L.aq = take(B * ns * ngi * kLimbBytes);
+  L.ae = take(B * ns * ngi * 8);
   L.d = take(B * ns * H * 4);
   L.nuniq = take(4);
   L.uniq_e = take((E + 1) * 4);
   L.uniq_off = take((E + 2) * 4);
   L.ent = take(B * ns * 4);
+  // published words of the single-token kernel (epoch << 32 | value)
+  L.pub_logits = take((E + 1) * 8);
+  L.pub_act = take(ns * I * 8);
   L.total = o;
   return L;
 }
@@ -100,7 +99,7 @@ size_t moe_workspace_bytes(const moe_dims* dims, int32_t max_batch) {
 }
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
-  if (!ws || !aligned16(ws) || ws_bytes < sizeof(WsHeader)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < kHeaderBytes) return MOE_ERR_INVALID_ARG;
   cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
@@ -174,17 +173,12 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int H = dims->hidden, I = dims->inter;
   WsHeader* hdr = at<WsHeader>(ws, 0);
-  const int lay = bits == 4 ? 1 : 2;
-
   NormQuantArgs nq{};
   nq.in = xn;
   nq.n = H;
   nq.do_norm = 0;
-  nq.layouts = lay;
-  nq.q4 = at<uint32_t>(ws, L.xq4);
-  nq.e4 = at<float2>(ws, L.xe4);
-  nq.q2 = at<uint32_t>(ws, L.xq2);
-  nq.e2 = at<float2>(ws, L.xe2);
+  nq.q = at<uint8_t>(ws, L.xq);
+  nq.e = at<float2>(ws, L.xe);
   nq.hdr = hdr;
   cudaError_t e = launch_norm_quant(nq, B, s);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -198,10 +192,8 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   g.bits = bits;
   g.shared_bits = bits;
   g.blob = static_cast<const uint8_t*>(blob);
-  g.xq4 = nq.q4;
-  g.xe4 = nq.e4;
-  g.xq2 = nq.q2;
-  g.xe2 = nq.e2;
+  g.xq = nq.q;
+  g.xe = nq.e;
   g.a_out = at<float>(ws, L.a);
   e = launch_gateup(g, 1, s);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -209,10 +201,8 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   NormQuantArgs aq = nq;
   aq.in = g.a_out;
   aq.n = I;
-  aq.q4 = at<uint32_t>(ws, L.aq4);
-  aq.e4 = at<float2>(ws, L.ae4);
-  aq.q2 = at<uint32_t>(ws, L.aq2);
-  aq.e2 = at<float2>(ws, L.ae2);
+  aq.q = at<uint8_t>(ws, L.aq);
+  aq.e = at<float2>(ws, L.ae);
   e = launch_norm_quant(aq, B, s);
   if (e != cudaSuccess) return cuda_fail(e);
 
@@ -225,10 +215,8 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   dn.bits = bits;
   dn.shared_bits = bits;
   dn.blob = g.blob;
-  dn.aq4 = aq.q4;
-  dn.ae4 = aq.e4;
-  dn.aq2 = aq.q2;
-  dn.ae2 = aq.e2;
+  dn.aq = aq.q;
+  dn.ae = aq.e;
   dn.d_out = at<float>(ws, L.d);
   e = launch_down(dn, 1, s);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -271,9 +259,10 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   cudaError_t e;
 
   if (B == 1 && !(d.flags & MOE_NO_FUSED)) {
-    FusedPlan plan;
-    if (fused_plan(d.hidden, d.inter, d.n_experts, d.top_k, d.bits, shared_bits, has_shared, current_device(), &plan)) {
-      FusedArgs f{};
+    DecodePlan plan;
+    if (decode_plan(d.hidden, d.inter, d.n_experts, d.top_k, d.bits, shared_bits, has_shared, has_gate,
+                    current_device(), &plan)) {
+      DecodeArgs f{};
       f.H = d.hidden;
       f.I = d.inter;
       f.E = d.n_experts;
@@ -294,10 +283,10 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
       f.idx_out = idx_out;
       f.w_out = w_out;
       f.hdr = hdr;
-      f.a_glob = at<float>(ws, L.a);
-      f.logits = at<float>(ws, L.logits);
+      f.pub_logits = at<unsigned long long>(ws, L.pub_logits);
+      f.pub_act = at<unsigned long long>(ws, L.pub_act);
       f.plan = plan;
-      e = launch_fused(f, s);
+      e = launch_decode(f, (d.flags & MOE_PDL) != 0, s);
       return e == cudaSuccess ? MOE_OK : cuda_fail(e);
     }
   }
@@ -305,7 +294,6 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   // multi-kernel path
   const int K = d.top_k, E = d.n_experts, H = d.hidden, I = d.inter;
   const int nslots = K + has_shared;
-  const int lay = ((d.bits == 4 || shared_bits == 4) ? 1 : 0) | ((d.bits == 2 || shared_bits == 2) ? 2 : 0);
   NormQuantArgs nq{};
   nq.in = h;
   nq.n = H;
@@ -313,11 +301,8 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   nq.eps = d.rms_eps;
   nq.gamma = layer->rms_gamma;
   nq.xn_out = at<float>(ws, L.xn);
-  nq.layouts = lay;
-  nq.q4 = at<uint32_t>(ws, L.xq4);
-  nq.e4 = at<float2>(ws, L.xe4);
-  nq.q2 = at<uint32_t>(ws, L.xq2);
-  nq.e2 = at<float2>(ws, L.xe2);
+  nq.q = at<uint8_t>(ws, L.xq);
+  nq.e = at<float2>(ws, L.xe);
   nq.hdr = hdr;
   if ((e = launch_norm_quant(nq, B, s)) != cudaSuccess) return cuda_fail(e);
 
@@ -374,10 +359,8 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   g.uniq_e = bk.uniq_e;
   g.uniq_off = bk.uniq_off;
   g.ent = bk.ent;
-  g.xq4 = nq.q4;
-  g.xe4 = nq.e4;
-  g.xq2 = nq.q2;
-  g.xe2 = nq.e2;
+  g.xq = nq.q;
+  g.xe = nq.e;
   g.a_out = at<float>(ws, L.a);
   if ((e = launch_gateup(g, items, s)) != cudaSuccess) return cuda_fail(e);
 
@@ -385,11 +368,8 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   aq.in = g.a_out;
   aq.n = I;
   aq.do_norm = 0;
-  aq.layouts = lay;
-  aq.q4 = at<uint32_t>(ws, L.aq4);
-  aq.e4 = at<float2>(ws, L.ae4);
-  aq.q2 = at<uint32_t>(ws, L.aq2);
-  aq.e2 = at<float2>(ws, L.ae2);
+  aq.q = at<uint8_t>(ws, L.aq);
+  aq.e = at<float2>(ws, L.ae);
   aq.hdr = hdr;
   if ((e = launch_norm_quant(aq, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
 
@@ -408,10 +388,8 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   dn.uniq_e = bk.uniq_e;
   dn.uniq_off = bk.uniq_off;
   dn.ent = bk.ent;
-  dn.aq4 = aq.q4;
-  dn.ae4 = aq.e4;
-  dn.aq2 = aq.q2;
-  dn.ae2 = aq.e2;
+  dn.aq = aq.q;
+  dn.ae = aq.e;
   dn.d_out = at<float>(ws, L.d);
   if ((e = launch_down(dn, items, s)) != cudaSuccess) return cuda_fail(e);
 
@@ -438,8 +416,10 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream) {
   WsHeader hh;
   e = cudaMemcpy(&hh, ws, sizeof(hh), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (hh.status || hh.abort) {
-    e = cudaMemset(ws, 0, sizeof(WsHeader));
+  if (hh.status || hh.abort || hh.bar_extra) {
+    // the error state only: the launch counter keeps counting, so that words
+    // published before the error can never match a later launch's epoch
+    e = cudaMemset(ws, 0, kHeaderErrorBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e);

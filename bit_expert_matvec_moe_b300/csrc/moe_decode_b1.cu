@@ -1,0 +1,611 @@
+// Single-token MoE layer in one launch of one block per SM.
+//
+// Block c of P owns gate/up row pairs [c*I/P, (c+1)*I/P) and down rows
+// [c*H/P, (c+1)*H/P) of every expert the token uses, and router rows
+// [c*E/P, (c+1)*E/P).  Its weight bytes arrive by bulk copies (TMA engine)
+// into shared memory, each with its own mbarrier:
+//   start         router rows, shared expert gate/up rows and down rows
+//   after top-K   gate/up rows of all K routed experts, then their down rows,
+//                 all issued at once (they fit beside each other)
+// Grid-wide data dependencies use split-phase barriers in the workspace header
+// (arrive when a block has published, wait only where the data is consumed):
+//   L     every block wrote its router logits          -> top-K
+//   S     every block wrote its slice of a_shared      -> shared down rows
+//   R_k   every block wrote its slice of a_k           -> routed down rows
+// Phases of a block:
+//   h -> limbs of h*gamma (the RMS factor r is applied to each dot product,
+//        so quantisation does not wait for the norm); r from a block sum
+//   router rows -> logits, arrive L
+//   shared gate/up + SwiGLU -> a_shared slice, arrive S
+//   wait L; top-K by one warp (every block, same result); issue routed copies
+//   routed gate/up + SwiGLU -> a_k slices, arrive R_k (as each expert lands)
+//   wait S and every R_k; limbs of every a; down rows of every expert -> y
+//   h[rows] += y
+// Routing never leaves the device.  Every wait is bounded (1 s): on timeout the
+// block records MOE_ERR_TIMEOUT, waits (bounded) for its own copies in flight
+// and leaves; later launches on the same workspace return at once until the
+// status word is read.  Nothing lives in local memory: with ~227 KB of shared
+// memory per block the L1 cache is small, and spilled state would go to L2.
+//
+// Limits of this kernel (the host falls back to the multi-kernel path outside
+// them): hidden <= 4096, inter <= 2048, experts <= 1024, top-K <= 8, and the
+// plan must fit in shared memory.
+//
+// With programmatic dependent launch (kPDL) the weight copies of the prologue
+// are issued before griddepcontrol.wait, i.e. while the previous kernel on the
+// stream may still run; nothing the caller writes (h, offsets, workspace) is
+// read before that wait.
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ int lo_row(int c, int P, int n) { return (int)((long long)c * n / P); }
+
+// Limbs of one group of 64 values held four per lane by a half-warp (lane j of
+// the half holds values 4j .. 4j+3); all 32 lanes of the warp must call it.
+// Each lane assembles three of the group's limb words; when `store`, it writes
+// them (limb vector `vec` of ng groups, group g) and lane 0 of the half writes
+// the group factors to *es.  Returns false when a value is not finite.
+__device__ __forceinline__ bool quantize_group4(float4 x, int lane, bool store, uint8_t* vec, int ng, int g,
+                                                float2* es) {
+  const int j = lane & 15;
+  float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const bool finite = isfinite(m);
+  int E = 0;
+  if (m > 0.f && finite) frexpf(m, &E);
+  E = max(E, -100);
+  const float up = __uint_as_float((uint32_t)(127 + 22 - E) << 23);  // 2^(22-E)
+  const float dn = __uint_as_float((uint32_t)(127 - 22 + E) << 23);  // 2^(E-22)
+  const int X0 = finite ? __float2int_rn(x.x * up) : 0;
+  const int X1 = finite ? __float2int_rn(x.y * up) : 0;
+  const int X2 = finite ? __float2int_rn(x.z * up) : 0;
+  const int X3 = finite ? __float2int_rn(x.w * up) : 0;
+  int s = X0 + X1 + X2 + X3;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  // word q = j >> 1 holds values 8q .. 8q+7; lane 2q has 8q..8q+3, lane 2q+1
+  // has 8q+4..8q+7.  The even lane builds the "even" limb words (values 8q,
+  // 8q+2, 8q+4, 8q+6), the odd lane the "odd" ones (8q+1, 8q+3, 8q+5, 8q+7).
+  const bool odd = j & 1;
+  const int gotA = __shfl_xor_sync(0xffffffffu, odd ? X0 : X1, 1);
+  const int gotB = __shfl_xor_sync(0xffffffffu, odd ? X2 : X3, 1);
+  const int v0 = odd ? gotA : X0, v1 = odd ? gotB : X2, v2 = odd ? X1 : gotA, v3 = odd ? X3 : gotB;
+  if (store) {
+    const int q = j >> 1;
+#pragma unroll
+    for (int l = 0; l < 3; ++l) {
+      const uint32_t word = ((uint32_t)(v0 >> (8 * l)) & 255u) | (((uint32_t)(v1 >> (8 * l)) & 255u) << 8) |
+                            (((uint32_t)(v2 >> (8 * l)) & 255u) << 16) | (((uint32_t)(v3 >> (8 * l)) & 255u) << 24);
+      const int w = 6 * q + 2 * l + (odd ? 1 : 0);
+      *reinterpret_cast<uint32_t*>(vec + ((size_t)(w >> 2) * ng + g) * 16 + (w & 3) * 4) = word;
+    }
+    if (j == 0) *es = make_float2(dn, (float)s * dn);
+  }
+  return finite;
+}
+
+// Dot products of one lane's group with up to two rows of a slice in shared
+// memory (rows r_first and r_first + step, those < nrows).  Row r starts at
+// base + (r >> 1) * 2 * stride + (r & 1) * stride for gate/up pairs, or
+// base + r * stride for down rows.  The lpr lanes of a row are reduced; every
+// lane of the row gets the row's partial over its chunk of groups.
+template <int BITS, bool kPairs>
+__device__ __forceinline__ void slice_rows2(const uint8_t* base, int stride, int codes, int ng, int g, bool gact,
+                                            const Limbs& L, float2 es, int r_first, int step, int nrows, int lpr,
+                                            float& out0, float& out1) {
+  float v[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int r = r_first + k * step;
+    v[k] = 0.f;
+    if (gact && r < nrows) {
+      const uint8_t* row = kPairs ? base + (size_t)(r >> 1) * (2 * stride) + (size_t)(r & 1) * stride
+                                  : base + (size_t)r * stride;
+      v[k] = row_group<BITS>(row, ng, codes, g, L, es);
+    }
+  }
+  out0 = row_reduce(v[0], lpr);
+  out1 = row_reduce(v[1], lpr);
+}
+
+}  // namespace
+
+template <bool kPDL>
+__global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a) {
+  // every piece of block scratch lives in the planned dynamic region, whose
+  // base is rounded up here to 128 bytes (the plan reserves the slack)
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* const sm = sm_raw + ((128u - (uint32_t)(__cvta_generic_to_shared(sm_raw) & 127u)) & 127u);
+
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int P = gridDim.x, c = blockIdx.x;
+  const int H = a.H, I = a.I, E = a.E, K = a.K, hs = a.has_shared;
+  const int NE = K + hs;
+  const int ngh = H / kGroup, ngi = I / kGroup;
+  const int r0 = lo_row(c, P, I), nr = lo_row(c + 1, P, I) - r0;
+  const int j0 = lo_row(c, P, H), nj = lo_row(c + 1, P, H) - j0;
+  const int e0 = lo_row(c, P, E), ne = lo_row(c + 1, P, E) - e0;
+  const int nrr = ne + ((a.has_gate && c == 0) ? 1 : 0);  // router rows of this block
+
+  // formats by value (4-bit and 2-bit), so that no per-expert choice needs memory
+  const Fmt f4 = make_fmt(4, H, I), f2 = make_fmt(2, H, I);
+  const int s_gu_pair = a.shared_bits == 4 ? f4.gu_pair : f2.gu_pair;
+  const int s_d_row = a.shared_bits == 4 ? f4.d_row : f2.d_row;
+  const size_t s_d_off = a.shared_bits == 4 ? f4.d_off : f2.d_off;
+  const int r_gu_pair = a.bits == 4 ? f4.gu_pair : f2.gu_pair;
+  const int r_d_row = a.bits == 4 ? f4.d_row : f2.d_row;
+  const size_t r_d_off = a.bits == 4 ? f4.d_off : f2.d_off;
+
+  uint8_t* const G = sm + a.plan.off_g;
+  uint8_t* const D = sm + a.plan.off_dn;
+  uint8_t* const AL = sm + a.plan.off_al;  // limbs: of x first, then of every weighted a
+  float2* const AE = reinterpret_cast<float2*>(sm + a.plan.off_ae);
+  float* const part = reinterpret_cast<float*>(sm + a.plan.off_part);    // [NE][part_stride]
+  float* const rpart = reinterpret_cast<float*>(sm + a.plan.off_rpart);  // [rows_r][kWarps]
+  float* const ysm = reinterpret_cast<float*>(sm + a.plan.off_y);        // [rows_d]
+  float* const pdn = reinterpret_cast<float*>(G);  // down partials [rows_d][NE * ngi], after the gate/up phase
+  uint64_t* const bar = reinterpret_cast<uint64_t*>(sm + a.plan.off_bar);
+  float* const s_red = reinterpret_cast<float*>(sm + a.plan.off_misc);               // [kWarps]
+  int* const s_idx = reinterpret_cast<int*>(sm + a.plan.off_misc + 64);              // [kMaxTopK]
+  float* const s_val = reinterpret_cast<float*>(sm + a.plan.off_misc + 96);          // [kMaxTopK]
+  float* const s_coef = reinterpret_cast<float*>(sm + a.plan.off_misc + 128);        // [kMaxTopK + 1]
+  uint32_t* const s_mask = reinterpret_cast<uint32_t*>(sm + a.plan.off_misc + 168);  // issued, failed, epoch, hook
+  const size_t gu_slot = a.plan.gu_slot, dn_slot = a.plan.dn_slot;
+  const int part_stride = a.plan.part_stride;
+  // mbarriers: [0] router rows, [1 + p] gate/up of expert p, [1 + NE + p] down
+  // of expert p, where expert p = 0 is the shared expert when present
+
+  // ---- prologue: barrier set-up, visible to every thread and to the copy
+  // engine before the first copy is issued
+  if (tid == 0) {
+    for (int i = 0; i < 1 + 2 * NE; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+    fence_proxy_async();
+    s_mask[0] = 0u;
+    s_mask[1] = 0u;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t issued = 0u;
+    if (nrr > 0) {
+      mbar_expect_tx(&bar[0], (uint32_t)nrr * H * 2);
+      uint8_t* rt = G + a.plan.off_rt;
+      if (ne > 0) bulk_g2s(rt, a.router + (size_t)e0 * H, (uint32_t)ne * H * 2, &bar[0]);
+      if (nrr > ne) bulk_g2s(rt + (size_t)ne * H * 2, a.gate, (uint32_t)H * 2, &bar[0]);
+      issued |= 1u;
+    }
+    if (hs) {
+      if (nr > 0) {
+        const uint32_t bytes = (uint32_t)nr * s_gu_pair;
+        mbar_expect_tx(&bar[1], bytes);
+        bulk_g2s(G + a.plan.off_sgu, a.shared + (size_t)r0 * s_gu_pair, bytes, &bar[1]);
+        issued |= 2u;
+      }
+      if (nj > 0) {
+        const uint32_t bytes = (uint32_t)nj * s_d_row;
+        mbar_expect_tx(&bar[1 + NE], bytes);
+        bulk_g2s(D, a.shared + s_d_off + (size_t)j0 * s_d_row, bytes, &bar[1 + NE]);
+        issued |= 2u << NE;
+      }
+    }
+    s_mask[0] = issued;
+  }
+  if (kPDL) {
+    pdl_launch_dependents();
+    pdl_wait_prior();
+  }
+
+  // one warp waits on mbarrier i (one phase per launch); a give-up is recorded
+  // and acted on at the next block barrier, so that all threads leave together
+  auto warp_wait = [&](int i) -> bool {
+    const bool ok = mbar_wait(&bar[i], 0);
+    if (!ok && lane == 0) atomicOr(&s_mask[1], 1u);
+    return __all_sync(0xffffffffu, ok);
+  };
+  auto failed = [&]() -> bool { return __syncthreads_or(tid == 0 && s_mask[1] != 0u) != 0; };
+
+  // ---- caller data and this launch's epoch, all in flight together
+  float4 hv0, hv1;
+  {
+    const float4* h4 = reinterpret_cast<const float4*>(a.h);
+    hv0 = 4 * tid < H ? h4[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
+    hv1 = 4 * (tid + kBlock) < H ? h4[tid + kBlock] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const float hres = tid < nj ? a.h[j0 + tid] : 0.f;
+  if (tid == 0) {
+    // every block of every launch adds one, so this launch is number count / P
+    const unsigned long long n = atomicAdd(&a.hdr->launches, 1ull);
+    s_mask[2] = (uint32_t)(n / (unsigned long long)P + 1ull);
+    s_mask[3] = *(volatile uint32_t*)&a.hdr->bar_extra;  // test hook: readers expect a later epoch
+  }
+  if (__syncthreads_or(tid == 0 && *(volatile uint32_t*)&a.hdr->abort)) goto cleanup;
+  {
+    const uint32_t epoch = s_mask[2];           // written with every published word
+    const uint32_t expect = epoch + s_mask[3];  // awaited by every reader
+
+    // ---- x = h * gamma; sum of h^2; limbs of x.  Thread t holds values
+    // 4t .. 4t+3 and 4(t+512) .. 4(t+512)+3, so warp w holds groups 2w, 2w+1
+    // of each pass; a pass is skipped by whole warps only.
+    float ss = 0.f;
+    bool finite = true;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i0 = 4 * (tid + kBlock * k);
+      float4 x = k == 0 ? hv0 : hv1;
+      ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, ss))));
+      if (a.gamma && i0 < H) {
+        const uint2 gw = *reinterpret_cast<const uint2*>(a.gamma + i0);
+        x.x *= bf16lo(gw.x); x.y *= bf16hi(gw.x); x.z *= bf16lo(gw.y); x.w *= bf16hi(gw.y);
+      }
+      if (k == 0) hv0 = x; else hv1 = x;
+      const int wbase = 4 * (32 * wid + kBlock * k);  // first value of this warp in this pass
+      if (wbase < H)
+        finite &= quantize_group4(x, lane, i0 < H, AL, ngh, i0 / kGroup, AE + i0 / kGroup);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) s_red[wid] = ss;
+    const int nonfinite_x = __syncthreads_or(!finite);
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += s_red[w];
+    const float rs = 1.0f / sqrtf(tot / (float)H + a.eps);  // xn = rs * x
+
+    // ---- gate/up lane geometry; this lane's limbs of x
+    const RowMap mh = make_rowmap(ngh);
+    const int gchunk = wid % mh.chunks, gnstreams = kWarps / mh.chunks;
+    const int gsub = lane % mh.lpr;
+    const int gg = gchunk * 32 + gsub;
+    const bool ggact = gg < ngh;
+    const int gr_warp = (wid / mh.chunks) * mh.rpp;  // first row of the warp (warp-uniform)
+    const int gr_first = gr_warp + lane / mh.lpr, gr_step = gnstreams * mh.rpp;
+    auto load_x = [&](Limbs& xl, float2& xe) {
+      xe = make_float2(0.f, 0.f);
+      if (ggact) {
+        load_limbs(AL, ngh, gg, xl);
+        xe = AE[gg];
+      } else {
+        zero_limbs(xl);
+      }
+    };
+    // gate/up rows of expert p (slice at `slot`, code width bits) -> partials
+    // part[p][r * chunks + chunk]; the warp waits for the slice itself.  The
+    // skip test is warp-uniform: the wait and the row reductions are warp
+    // collectives, so a warp takes part with all of its lanes or not at all.
+    auto gate_up = [&](int p, const uint8_t* slot, int bits, const Limbs& xl, float2 xe) {
+      if (nr == 0 || gr_warp >= 2 * nr) return;  // no rows for this warp: nothing to wait for
+      if (!warp_wait(1 + p)) return;
+      float o0, o1;
+      if (bits == 4)
+        slice_rows2<4, true>(slot, f4.gu_row, f4.gu_codes, ngh, gg, ggact, xl, xe, gr_first, gr_step, 2 * nr,
+                             mh.lpr, o0, o1);
+      else
+        slice_rows2<2, true>(slot, f2.gu_row, f2.gu_codes, ngh, gg, ggact, xl, xe, gr_first, gr_step, 2 * nr,
+                             mh.lpr, o0, o1);
+      if (gsub == 0) {
+        float* pb = part + (size_t)p * part_stride;
+        if (gr_first < 2 * nr) pb[gr_first * mh.chunks + gchunk] = o0;
+        if (gr_first + gr_step < 2 * nr) pb[(gr_first + gr_step) * mh.chunks + gchunk] = o1;
+      }
+    };
+
+    // ---- router rows -> published logits (each thread's 8 values of x against each row)
+    if (nrr > 0) warp_wait(0);
+    {
+      const uint8_t* rt = G + a.plan.off_rt;
+      for (int ri = 0; ri < nrr; ++ri) {
+        float acc = 0.f;
+        if (4 * tid < H) {
+          const uint2 rw = *reinterpret_cast<const uint2*>(rt + ((size_t)ri * H + 4 * tid) * 2);
+          acc = fmaf(bf16lo(rw.x), hv0.x, acc);
+          acc = fmaf(bf16hi(rw.x), hv0.y, acc);
+          acc = fmaf(bf16lo(rw.y), hv0.z, acc);
+          acc = fmaf(bf16hi(rw.y), hv0.w, acc);
+        }
+        if (4 * (tid + kBlock) < H) {
+          const uint2 rw = *reinterpret_cast<const uint2*>(rt + ((size_t)ri * H + 4 * (tid + kBlock)) * 2);
+          acc = fmaf(bf16lo(rw.x), hv1.x, acc);
+          acc = fmaf(bf16hi(rw.x), hv1.y, acc);
+          acc = fmaf(bf16lo(rw.y), hv1.z, acc);
+          acc = fmaf(bf16hi(rw.y), hv1.w, acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) rpart[ri * kWarps + wid] = acc;
+      }
+    }
+    if (failed()) goto cleanup;
+    if (tid < nrr) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += rpart[tid * kWarps + w];
+      v *= rs;
+      const int e = tid < ne ? e0 + tid : E;  // the shared-gate logit is row E
+      if (e < E && a.offset) v += a.offset[e];
+      st_pub(a.pub_logits + e, v, epoch);
+    }
+
+    // ---- shared expert gate/up (its rows were staged first)
+    if (hs) {
+      Limbs xl;
+      float2 xe;
+      load_x(xl, xe);
+      gate_up(0, G + a.plan.off_sgu, a.shared_bits, xl, xe);
+    }
+    {
+      // ---- routing, by warp 0 of every block (same logits, same result); the
+      // other warps go on to wait for the routed rows.  The routed copies
+      // overwrite the gate/up area, so warp 0 issues them only after every
+      // warp has finished with the shared rows (named barrier 1: the other
+      // warps arrive without waiting).
+      if (wid != 0) named_arrive(1, kBlock);
+      if (wid == 0) {
+        named_sync(1, kBlock);
+        bool ok = true, ready = true;
+        uint32_t key[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) key[i] = 0u;
+        // published logits of this launch: lane l polls experts l, l + 32, ...
+        const int mine = E > lane ? (E - lane + 31) / 32 : 0;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          if (ch * 8 < mine && ready) {  // lane-dependent, no collectives inside
+            float v[8];
+            ready = poll_pub<8>(a.hdr, a.pub_logits + lane + 256 * ch, 32, min(8, mine - ch * 8), expect, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (ch * 8 + i < mine) {
+                ok &= isfinite(v[i]);
+                key[ch * 8 + i] = fkey(v[i]);
+              }
+            }
+          }
+        }
+        float gate_logit = 0.f;
+        if (lane == 0 && a.has_gate && ready) {
+          float v[1];
+          ready = poll_pub<1>(a.hdr, a.pub_logits + E, 1, 1, expect, v);
+          gate_logit = v[0];
+        }
+        if (__all_sync(0xffffffffu, ready)) {
+          if (E <= 128) {
+            uint32_t k4[4] = {key[0], key[1], key[2], key[3]};
+            warp_topk<4>(k4, K, lane, s_idx, s_val);
+          } else if (E <= 512) {
+            uint32_t k16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) k16[i] = key[i];
+            warp_topk<16>(k16, K, lane, s_idx, s_val);
+          } else {
+            warp_topk<32>(key, K, lane, s_idx, s_val);
+          }
+          ok = __all_sync(0xffffffffu, ok);
+          if (lane == 0) {
+            // the generic-proxy reads of the gate/up area are complete (block
+            // barrier after the router rows, named barrier after the shared rows)
+            fence_proxy_async();
+            uint32_t issued = s_mask[0];
+            for (int k = 0; k < K; ++k) {
+              const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
+              if (nr > 0) {
+                const uint32_t bytes = (uint32_t)nr * r_gu_pair;
+                mbar_expect_tx(&bar[1 + hs + k], bytes);
+                bulk_g2s(G + (size_t)k * gu_slot, blob + (size_t)r0 * r_gu_pair, bytes, &bar[1 + hs + k]);
+                issued |= 2u << (hs + k);
+              }
+            }
+            for (int k = 0; k < K; ++k) {
+              const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
+              if (nj > 0) {
+                const uint32_t bytes = (uint32_t)nj * r_d_row;
+                mbar_expect_tx(&bar[1 + NE + hs + k], bytes);
+                bulk_g2s(D + (size_t)(hs + k) * dn_slot, blob + r_d_off + (size_t)j0 * r_d_row, bytes,
+                         &bar[1 + NE + hs + k]);
+                issued |= 2u << (NE + hs + k);
+              }
+            }
+            s_mask[0] = issued;
+            chosen_softmax(s_val, K, s_coef + hs);
+            if (hs) s_coef[0] = a.has_gate ? 1.0f / (1.0f + expf(-gate_logit)) : 1.0f;
+            if (c == 0) {
+              if (!ok || nonfinite_x) atomicOr(&a.hdr->status, ST_NONFINITE);
+              for (int k = 0; k < K; ++k) {
+                if (a.idx_out) a.idx_out[k] = s_idx[k];
+                if (a.w_out) a.w_out[k] = s_coef[hs + k];
+              }
+            }
+          }
+        } else if (lane == 0) {
+          atomicOr(&s_mask[1], 1u);
+        }
+        __syncwarp();
+      }
+    }
+    {
+      // ---- routed gate/up rows, in the order the copies were issued
+      Limbs xl;
+      float2 xe;
+      load_x(xl, xe);
+      for (int k = 0; k < K; ++k) gate_up(hs + k, G + (size_t)k * gu_slot, a.bits, xl, xe);
+    }
+
+    // ---- SwiGLU of every expert's rows, weighted by the expert's routing
+    // coefficient, published for every block
+    if (failed()) goto cleanup;
+    for (int t = tid; t < NE * nr; t += kBlock) {
+      const int p = t / nr, i = t - p * nr;
+      const float* pb = part + (size_t)p * part_stride;
+      float gsum = 0.f, usum = 0.f;
+      for (int ch = 0; ch < mh.chunks; ++ch) {
+        gsum += pb[(2 * i) * mh.chunks + ch];
+        usum += pb[(2 * i + 1) * mh.chunks + ch];
+      }
+      st_pub(a.pub_act + (size_t)p * I + r0 + i, s_coef[p] * silu_mul(rs * gsum, rs * usum), epoch);
+    }
+
+    // ---- limbs of every weighted a: a half-warp per group, 2 groups per warp per pass
+    {
+      bool fin = true, ready = true;
+      const int ngroups = NE * ngi;
+      for (int base = 2 * wid; base < ngroups; base += 2 * kWarps) {
+        const int gi = base + (lane >> 4);
+        const bool real = gi < ngroups;
+        const int gq = real ? gi : base;  // the idle half takes part in the shuffles
+        const int p = gq / ngi, g = gq - p * ngi;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ready) ready = poll_pub<4>(a.hdr, a.pub_act + (size_t)p * I + g * kGroup + 4 * (lane & 15), 1, 4, expect, v);
+        const bool f = quantize_group4(make_float4(v[0], v[1], v[2], v[3]), lane, real,
+                                       AL + (size_t)p * ngi * kLimbBytes, ngi, g, AE + (size_t)p * ngi + g);
+        fin &= f || !real;
+      }
+      if (!ready) atomicOr(&s_mask[1], 1u);
+      if (__syncthreads_or(!fin) && tid == 0) atomicOr(&a.hdr->status, ST_NONFINITE);
+    }
+    if (failed()) goto cleanup;
+
+    // ---- down rows of every expert as one long dot product per row: thread
+    // (set, q) takes unit q = (expert p, group g) of rows set, set + S, ...;
+    // partials go to pdn[row][q] and are summed in a fixed order
+    {
+      const int Q = NE * ngi, S = kBlock / Q;
+      const int set = tid / Q, q = tid - set * Q;
+      if (set < S && set < nj) {
+        const int p = q / ngi, g = q - p * ngi;
+        // lanes of one warp may belong to different experts: each thread waits
+        // for its own expert's rows (no warp collective in this section)
+        if (!mbar_wait(&bar[1 + NE + p], 0)) atomicOr(&s_mask[1], 1u);
+        Limbs L;
+        load_limbs(AL + (size_t)p * ngi * kLimbBytes, ngi, g, L);
+        const float2 es = AE[(size_t)p * ngi + g];
+        const uint8_t* base = D + (size_t)p * dn_slot;
+        const bool b4 = (p < hs ? a.shared_bits : a.bits) == 4;
+        for (int r = set; r < nj; r += S) {
+          const float v = b4 ? row_group<4>(base + (size_t)r * f4.d_row, ngi, f4.d_codes, g, L, es)
+                             : row_group<2>(base + (size_t)r * f2.d_row, ngi, f2.d_codes, g, L, es);
+          pdn[r * Q + q] = v;
+        }
+      }
+      if (failed()) goto cleanup;
+      // row r: 16 threads sum every 16th partial, then a butterfly over the 16
+      {
+        const int r = tid >> 4, sub = tid & 15;
+        float v = 0.f;
+        if (r < nj)
+          for (int qq = sub; qq < Q; qq += 16) v += pdn[r * Q + qq];
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (sub == 0 && r < nj) ysm[r] = v;
+      }
+      __syncthreads();
+      if (tid < nj) a.h[j0 + tid] = hres + ysm[tid];
+    }
+  }
+  return;
+
+cleanup:
+  // leave only after this block's own copies in flight have landed
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t issued = s_mask[0];
+    for (int i = 0; i < 1 + 2 * NE; ++i)
+      if (issued >> i & 1u) mbar_wait(&bar[i], 0);
+  }
+  __syncthreads();
+}
+
+bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, int shared_bits, int has_shared,
+                     int has_gate, DecodePlan* out) {
+  const int NE = K + has_shared;
+  if (H > 4096 || I > 2048 || E > 1024 || K > kMaxTopK || nsm < 1) return false;
+  const Fmt fr = make_fmt(bits, H, I);
+  const Fmt fs = make_fmt(has_shared ? shared_bits : bits, H, I);
+  const RowMap mh = make_rowmap(fr.ng_h), mi = make_rowmap(fr.ng_i);
+  if (kWarps % mh.chunks || mi.chunks != 1) return false;
+  DecodePlan p{};
+  p.P = nsm;
+  p.rows_gu = (I + nsm - 1) / nsm;
+  p.rows_d = (H + nsm - 1) / nsm;
+  p.rows_r = (E + nsm - 1) / nsm + (has_gate ? 1 : 0);
+  // each warp covers at most two gate/up rows and two down rows per expert;
+  // SwiGLU rows and router rows are finished by one warp
+  if (2 * p.rows_gu > 2 * (kWarps / mh.chunks) * mh.rpp) return false;
+  if (p.rows_d > 2 * kWarps * mi.rpp) return false;
+  if (p.rows_gu > 32 || p.rows_r > 32 || p.rows_d > kBlock / 16) return false;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = (o + bytes + 127) & ~size_t(127);
+    return at;
+  };
+  // down slices, one slot per expert (slot 0 the shared expert when present)
+  p.dn_slot = pad16((size_t)p.rows_d * std::max(fr.d_row, fs.d_row));
+  p.off_dn = take((size_t)NE * p.dn_slot);
+  // gate/up area: the K routed slices, or (before routing) the shared slice
+  // and the router rows (offsets relative to the area)
+  p.gu_slot = pad16((size_t)p.rows_gu * fr.gu_pair);
+  size_t pre = 0;
+  auto sub = [&](size_t bytes) {
+    const size_t at = pre;
+    pre = (pre + bytes + 127) & ~size_t(127);
+    return at;
+  };
+  p.off_sgu = sub(has_shared ? (size_t)p.rows_gu * fs.gu_pair : 0);
+  p.off_rt = sub((size_t)p.rows_r * H * 2);
+  // after the gate/up phase the area also holds the down partials [rows_d][NE * ng_i]
+  p.off_g = take(std::max(std::max(pre, (size_t)K * p.gu_slot), (size_t)p.rows_d * NE * fr.ng_i * 4));
+  // limbs: of x first (read into registers), later of every expert's activation
+  const size_t ngroups = std::max((size_t)NE * fr.ng_i, (size_t)fr.ng_h);
+  p.off_al = take(ngroups * kLimbBytes);
+  p.off_ae = take(ngroups * 8);
+  p.part_stride = 2 * p.rows_gu * mh.chunks;
+  p.off_part = take((size_t)NE * p.part_stride * 4);
+  p.off_rpart = take((size_t)p.rows_r * kWarps * 4);
+  p.off_y = take((size_t)p.rows_d * 4);
+  p.off_bar = take((size_t)(1 + 2 * NE) * 8);
+  p.off_misc = take(256);
+  p.total = o + 128;  // slack for rounding the dynamic base up to 128 bytes
+  if (p.total > (size_t)optin) return false;
+  *out = p;
+  return true;
+}
+
+bool decode_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_shared, int has_gate, int device,
+                 DecodePlan* out) {
+  int nsm = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) return false;
+  return decode_plan_for(nsm, optin, H, I, E, K, bits, shared_bits, has_shared, has_gate, out);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s) {
+  static int configured_bytes[2] = {-1, -1};
+  const int bytes = (int)a.plan.total;
+  if (bytes > 48 * 1024 && bytes > configured_bytes[pdl]) {
+    cudaError_t e = pdl ? cudaFuncSetAttribute(decode_b1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+                        : cudaFuncSetAttribute(decode_b1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    configured_bytes[pdl] = bytes;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.plan.P);
+  cfg.blockDim = dim3(kBlock);
+  cfg.dynamicSmemBytes = (size_t)bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    // one block per SM (shared memory forces it) and one wave: every block is
+    // resident once the previous kernel's blocks have left
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return pdl ? cudaLaunchKernelEx(&cfg, decode_b1_kernel<true>, a) : cudaLaunchKernelEx(&cfg, decode_b1_kernel<false>, a);
+}
+
+}  // namespace moe

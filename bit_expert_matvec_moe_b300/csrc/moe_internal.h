@@ -11,9 +11,10 @@
 namespace moe {
 
 constexpr int kBlock = 512;   // threads per block of the matvec kernels
+constexpr int kWarps = kBlock / 32;
 constexpr int kRowsGU = 8;    // gate/up row pairs per block (multi-kernel path)
 constexpr int kRowsD = 32;    // down rows per block (multi-kernel path)
-constexpr int kMaxSlots = 3;  // gate/up staging ring of the fused kernel
+
 
 struct PackArgs {
   Fmt f;
@@ -30,11 +31,8 @@ struct NormQuantArgs {
   float eps;
   const uint16_t* gamma;
   float* xn_out;
-  int layouts;  // bit 0: 4-bit limb order, bit 1: 2-bit limb order
-  uint32_t* q4;
-  float2* e4;
-  uint32_t* q2;
-  float2* e2;
+  uint8_t* q;   // limb vectors [rows][ng * kLimbBytes]
+  float2* e;    // [rows][ng]
   WsHeader* hdr;
 };
 
@@ -79,10 +77,8 @@ struct GateUpArgs {
   const int* uniq_e;
   const int* uniq_off;
   const int* ent;
-  const uint32_t* xq4;
-  const float2* xe4;
-  const uint32_t* xq2;
-  const float2* xe2;
+  const uint8_t* xq;   // limbs of each token's xn
+  const float2* xe;
   float* a_out;  // [B * nslots, I]
 };
 
@@ -97,10 +93,8 @@ struct DownArgs {
   const int* uniq_e;
   const int* uniq_off;
   const int* ent;
-  const uint32_t* aq4;
-  const float2* ae4;
-  const uint32_t* aq2;
-  const float2* ae2;
+  const uint8_t* aq;   // limbs of each (token, slot) activation
+  const float2* ae;
   float* d_out;  // [B * nslots, H]
 };
 
@@ -113,18 +107,24 @@ struct CombineArgs {
   float* out;
 };
 
-// Shared-memory plan of the fused single-token kernel (byte offsets).
-struct FusedPlan {
-  int P;           // grid size (co-resident blocks)
-  int nslots;      // gate/up staging slots
-  int rows_gu;     // max gate/up row pairs per block
-  int rows_d;      // max down rows per block
-  size_t slot_bytes;
-  size_t off_x, off_xq4, off_xq2, off_xe4, off_xe2, off_ae, off_gu, off_dn[kMaxTopK + 1], off_part, off_pd,
-      off_logits, off_bar, total;
+// Shared-memory plan of the single-token kernel (byte offsets into dynamic smem).
+struct DecodePlan {
+  int P;            // grid size: one block per SM
+  int rows_gu;      // max gate/up row pairs per block
+  int rows_d;       // max down rows per block
+  int rows_r;       // max router rows per block (incl. the shared-gate row)
+  int part_stride;  // floats per gate/up partial buffer
+  size_t gu_slot;   // bytes of one routed expert's gate/up slice
+  size_t dn_slot;   // bytes of one expert's down slice
+  size_t off_dn;    // down slices, slot p at off_dn + p * dn_slot
+  size_t off_g;     // gate/up area (before routing: shared slice, router rows)
+  size_t off_sgu, off_rt;  // relative to off_g
+  size_t off_al, off_ae;   // limbs of x, later of every expert's activation
+  size_t off_part, off_rpart, off_y, off_bar, off_misc;
+  size_t total;
 };
 
-struct FusedArgs {
+struct DecodeArgs {
   int H, I, E, K, bits, shared_bits, has_shared, has_gate;
   float eps;
   const uint8_t* experts;
@@ -138,9 +138,9 @@ struct FusedArgs {
   int32_t* idx_out;
   float* w_out;
   WsHeader* hdr;
-  float* a_glob;   // [(K + 1), I]
-  float* logits;   // [E + 1]
-  FusedPlan plan;
+  unsigned long long* pub_logits;  // [E + 1] published words
+  unsigned long long* pub_act;     // [(K + 1), I] published words (weighted activations)
+  DecodePlan plan;
 };
 
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t s);
@@ -152,8 +152,11 @@ cudaError_t launch_gateup(const GateUpArgs& a, int items, cudaStream_t s);
 cudaError_t launch_down(const DownArgs& a, int items, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 
-// Fused single-token layer: plan (false when the shape does not fit) and launch.
-bool fused_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_shared, int device, FusedPlan* out);
-cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
+// Single-token layer: plan (false when the shape does not fit) and launch.
+bool decode_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_shared, int has_gate, int device,
+                 DecodePlan* out);
+bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, int shared_bits, int has_shared,
+                     int has_gate, DecodePlan* out);
+cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s);
 
 }  // namespace moe

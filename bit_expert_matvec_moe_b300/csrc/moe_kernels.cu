@@ -1,6 +1,6 @@
 // Multi-kernel MoE path (any batch) and the kernels behind moe_pack_weights,
 // moe_route and moe_expert_forward.  The single-token layer has its own fused
-// persistent kernel (moe_fused.cu); both use the device blocks of moe_device.cuh.
+// kernel (moe_decode_b1.cu); both use the device blocks of moe_device.cuh.
 #include "moe_internal.h"
 
 namespace moe {
@@ -9,8 +9,31 @@ namespace moe {
 // moe_pack_weights: canonical (codes, scales, biases) x 3 -> one blob
 // ---------------------------------------------------------------------------
 // One thread per 4-byte word of the blob.  Gate row i and up row i sit side by
-// side (one activation read serves both), each row is its codes followed by one
-// (scale | bias << 16) word per group, padded to 16 bytes; down rows follow.
+// side (one activation read serves both), each row is its codes (in the order
+// described in moe_device.cuh) followed by one (scale | bias << 16) word per
+// group, padded to 16 bytes; down rows follow.
+__device__ __forceinline__ uint32_t packed_code_word(const uint8_t* crow, int bits, int ng, int o) {
+  if (bits == 4) {
+    // output byte o: chunk k of up to 32 groups, half h, chunk-local group i
+    const int k = o >> 10, rem = o & 1023;
+    const int n = min(32, ng - 32 * k);
+    const int h = rem / (16 * n), i = (rem % (16 * n)) >> 4, jb = rem & 15;
+    const int g = 32 * k + i;
+    return *reinterpret_cast<const uint32_t*>(crow + 32 * g + 16 * h + jb);
+  }
+  // 2-bit: word o/4 of the row holds inputs 16m..16m+15 (m = o/4); field t of
+  // byte j takes input 16m + P(j, t), P = {2j, 2j+1, 8+2j, 9+2j}
+  const uint32_t cw = *reinterpret_cast<const uint32_t*>(crow + o);  // canonical: input u at bits 2u
+  uint32_t out = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int u[4] = {2 * j, 2 * j + 1, 8 + 2 * j, 9 + 2 * j};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) out |= ((cw >> (2 * u[t])) & 3u) << (8 * j + 2 * t);
+  }
+  return out;
+}
+
 __global__ void pack_kernel(PackArgs a) {
   const Fmt f = a.f;
   const size_t nwords = f.total / 4;
@@ -34,7 +57,7 @@ __global__ void pack_kernel(PackArgs a) {
     }
     uint32_t v = 0u;
     if (inrow < codes_bytes) {
-      v = *reinterpret_cast<const uint32_t*>(a.codes[m] + (size_t)row * codes_bytes + inrow);
+      v = packed_code_word(a.codes[m] + (size_t)row * codes_bytes, f.bits, ng, inrow);
     } else if (inrow < codes_bytes + 4 * ng) {
       const int g = (inrow - codes_bytes) / 4;
       v = (uint32_t)a.scales[m][(size_t)row * ng + g] | ((uint32_t)a.biases[m][(size_t)row * ng + g] << 16);
@@ -47,8 +70,8 @@ __global__ void pack_kernel(PackArgs a) {
 // RMSNorm (optional) + limbs of each token vector
 // ---------------------------------------------------------------------------
 // grid = B, block = kBlock.  in fp32 [B, n]; when do_norm, xn = in * rsqrt(mean(in^2)+eps) * gamma
-// is written to xn_out; the limbs of (do_norm ? xn : in) are written for the code
-// widths in `layouts` (bit 0: 4-bit order to q4, bit 1: 2-bit order to q2).
+// is written to xn_out; the limbs of (do_norm ? xn : in) go to q (row b at
+// q + b * ng * 128 bytes) and the group factors to e.
 __global__ void __launch_bounds__(kBlock) norm_quant_kernel(NormQuantArgs a) {
   extern __shared__ float4 nq_smem[];
   float* v = reinterpret_cast<float*>(nq_smem);
@@ -82,11 +105,10 @@ __global__ void __launch_bounds__(kBlock) norm_quant_kernel(NormQuantArgs a) {
   __syncthreads();
   const int ng = a.n / kGroup;
   bool ok = true;
+  uint8_t* qb = a.q + (size_t)b * ng * kLimbBytes;
   for (int g = wid; g < ng; g += blockDim.x >> 5) {
     const float x0 = v[g * kGroup + 2 * lane], x1 = v[g * kGroup + 2 * lane + 1];
-    const size_t gi = (size_t)b * ng + g;
-    if (a.layouts & 1) ok &= quantize_group<4>(x0, x1, lane, reinterpret_cast<uint8_t*>(a.q4 + gi * kLimbWords), a.e4 + gi);
-    if (a.layouts & 2) ok &= quantize_group<2>(x0, x1, lane, reinterpret_cast<uint8_t*>(a.q2 + gi * kLimbWords), a.e2 + gi);
+    ok &= quantize_group(x0, x1, lane, qb + 16 * g, 16 * ng, a.e + (size_t)b * ng + g);
   }
   if (!ok && lane == 0) atomicOr(&a.hdr->status, ST_NONFINITE);
 }
@@ -138,32 +160,40 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// softmax / top-K / renormalise per token
+// softmax / top-K / renormalise per token: one warp per token
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBlock) topk_kernel(TopkArgs a) {
-  extern __shared__ float4 tk_smem[];
-  float* lg = reinterpret_cast<float*>(tk_smem);
-  __shared__ unsigned long long cand[(kBlock / 32) * kMaxTopK];
-  __shared__ int sidx[kMaxTopK];
-  __shared__ float sw[kMaxTopK];
-  __shared__ int flag;
-  const int b = blockIdx.x;
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) lg[e] = a.logits[(size_t)b * (a.E + 1) + e];
-  __syncthreads();
-  const bool ok = block_topk(lg, a.E, a.K, cand, sidx, sw, &flag);
-  if (threadIdx.x < a.K) {
-    const int k = threadIdx.x;
-    a.idx[(size_t)b * a.K + k] = sidx[k];
-    a.w[(size_t)b * a.K + k] = sw[k];
-    if (a.idx_out) a.idx_out[(size_t)b * a.K + k] = sidx[k];
-    if (a.w_out) a.w_out[(size_t)b * a.K + k] = sw[k];
+constexpr int kTopkPer = 32;  // experts per lane: up to 1024 experts
+__global__ void __launch_bounds__(32) topk_kernel(TopkArgs a) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const float* lg = a.logits + (size_t)b * (a.E + 1);
+  uint32_t key[kTopkPer];
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < kTopkPer; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = 0u;
+    if (e < a.E) {
+      const float v = lg[e];
+      finite &= isfinite(v);
+      key[i] = fkey(v);
+      if (a.logits_out) a.logits_out[(size_t)b * a.E + e] = v;
+    }
   }
-  if (threadIdx.x == 0) {
-    if (a.gs) a.gs[b] = a.has_gate ? 1.0f / (1.0f + expf(-a.logits[(size_t)b * (a.E + 1) + a.E])) : 1.0f;
+  __shared__ int s_idx[kMaxTopK];
+  __shared__ float s_val[kMaxTopK], s_w[kMaxTopK];
+  warp_topk<kTopkPer>(key, a.K, lane, s_idx, s_val);
+  const bool ok = __all_sync(0xffffffffu, finite);
+  if (lane == 0) {
+    chosen_softmax(s_val, a.K, s_w);
+    for (int k = 0; k < a.K; ++k) {
+      a.idx[(size_t)b * a.K + k] = s_idx[k];
+      a.w[(size_t)b * a.K + k] = s_w[k];
+      if (a.idx_out) a.idx_out[(size_t)b * a.K + k] = s_idx[k];
+      if (a.w_out) a.w_out[(size_t)b * a.K + k] = s_w[k];
+    }
+    if (a.gs) a.gs[b] = a.has_gate ? 1.0f / (1.0f + expf(-lg[a.E])) : 1.0f;
     if (!ok) atomicOr(&a.hdr->status, ST_NONFINITE);
   }
-  if (a.logits_out)
-    for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.logits_out[(size_t)b * a.E + e] = lg[e];
 }
 
 // ---------------------------------------------------------------------------
@@ -217,14 +247,49 @@ __global__ void __launch_bounds__(kBlock) bucket_kernel(BucketArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// dot products of `nrows` quantised rows with one activation vector
+// ---------------------------------------------------------------------------
+//   rows      row r starts at rows + row_off(r) (codes, then one (s,b) word per group)
+//   xq, xe    the vector's limbs (ng groups, layout of moe_device.cuh) and factors
+//   part      out: part[r * chunks + chunk] = partial dot over the chunk's groups
+// All warps of the block take part; the caller syncs after.
+template <int BITS, typename RowOff>
+__device__ __forceinline__ void rows_dot(const uint8_t* rows, RowOff row_off, int nrows, int ng, int codes_bytes,
+                                         const uint8_t* xq, const float2* xe, float* part, int wi, int nw, int lane) {
+  const RowMap m = make_rowmap(ng);
+  const int chunk = wi % m.chunks;
+  const int stream = wi / m.chunks;
+  const int nstreams = nw / m.chunks;
+  if (stream >= nstreams) return;
+  const int sub = lane % m.lpr, slot = lane / m.lpr;
+  const int g = chunk * 32 + sub;
+  const bool gact = g < ng;
+  Limbs L;
+  float2 es = make_float2(0.f, 0.f);
+  if (gact) {
+    load_limbs(xq, ng, g, L);
+    es = xe[g];
+  } else {
+    zero_limbs(L);
+  }
+  const int step = nstreams * m.rpp;
+  for (int base = stream * m.rpp; base < nrows; base += step) {
+    const int r = base + slot;
+    float v = 0.f;
+    if (gact && r < nrows) v = row_group<BITS>(rows + row_off(r), ng, codes_bytes, g, L, es);
+    v = row_reduce(v, m.lpr);
+    if (sub == 0 && r < nrows) part[r * m.chunks + chunk] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // grouped gate/up + SwiGLU: a[b][slot][r] = silu(Wg_r . xn_b) * (Wu_r . xn_b)
 // ---------------------------------------------------------------------------
 // grid = (row blocks of kRowsGU gate/up row pairs, work items); block = kBlock.
 // Item u is expert uniq_e[u] (or the shared expert) with its token entries.
 // Without a list (single-expert mode) the item is `blob` with tokens 0..B-1.
 template <int BITS>
-__device__ void gateup_item(const GateUpArgs& a, const uint8_t* blob, const Fmt& f, const int* ent, int nent,
-                            const uint32_t* xq, const float2* xe) {
+__device__ void gateup_item(const GateUpArgs& a, const uint8_t* blob, const Fmt& f, const int* ent, int nent) {
   __shared__ float part[2 * kRowsGU * 4];  // up to 4 chunks (hidden <= 8192)
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int r0 = blockIdx.x * kRowsGU;
@@ -236,8 +301,8 @@ __device__ void gateup_item(const GateUpArgs& a, const uint8_t* blob, const Fmt&
   for (int t = 0; t < nent; ++t) {
     const int e = ent ? ent[t] : t * a.nslots;  // b * nslots + slot
     const int b = e / a.nslots;
-    rows_dot<BITS>(rows, off, 2 * nr, f.ng_h, f.gu_codes, xq + (size_t)b * f.ng_h * kLimbWords, xe + (size_t)b * f.ng_h,
-                   part, wid, nw, lane);
+    rows_dot<BITS>(rows, off, 2 * nr, f.ng_h, f.gu_codes, a.xq + (size_t)b * f.ng_h * kLimbBytes,
+                   a.xe + (size_t)b * f.ng_h, part, wid, nw, lane);
     __syncthreads();
     if ((int)threadIdx.x < nr) {
       const int r = threadIdx.x;
@@ -273,17 +338,16 @@ __global__ void __launch_bounds__(kBlock) gateup_kernel(GateUpArgs a) {
   }
   const Fmt f = make_fmt(bits, a.H, a.I);
   if (bits == 4)
-    gateup_item<4>(a, blob, f, ent, nent, a.xq4, a.xe4);
+    gateup_item<4>(a, blob, f, ent, nent);
   else
-    gateup_item<2>(a, blob, f, ent, nent, a.xq2, a.xe2);
+    gateup_item<2>(a, blob, f, ent, nent);
 }
 
 // ---------------------------------------------------------------------------
 // grouped down: d[b][slot][j] = Wd_j . a[b][slot]
 // ---------------------------------------------------------------------------
 template <int BITS>
-__device__ void down_item(const DownArgs& a, const uint8_t* blob, const Fmt& f, const int* ent, int nent,
-                          const uint32_t* aq, const float2* ae) {
+__device__ void down_item(const DownArgs& a, const uint8_t* blob, const Fmt& f, const int* ent, int nent) {
   __shared__ float part[kRowsD * 4];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int j0 = blockIdx.x * kRowsD;
@@ -294,8 +358,8 @@ __device__ void down_item(const DownArgs& a, const uint8_t* blob, const Fmt& f, 
   auto off = [&](int r) { return (size_t)r * f.d_row; };
   for (int t = 0; t < nent; ++t) {
     const int e = ent ? ent[t] : t * a.nslots;
-    rows_dot<BITS>(rows, off, nr, f.ng_i, f.d_codes, aq + (size_t)e * f.ng_i * kLimbWords, ae + (size_t)e * f.ng_i, part,
-                   wid, nw, lane);
+    rows_dot<BITS>(rows, off, nr, f.ng_i, f.d_codes, a.aq + (size_t)e * f.ng_i * kLimbBytes, a.ae + (size_t)e * f.ng_i,
+                   part, wid, nw, lane);
     __syncthreads();
     for (int r = threadIdx.x; r < nr; r += blockDim.x) {
       float s = 0.f;
@@ -325,11 +389,10 @@ __global__ void __launch_bounds__(kBlock) down_kernel(DownArgs a) {
     nent = a.uniq_off[item + 1] - a.uniq_off[item];
   }
   const Fmt f = make_fmt(bits, a.H, a.I);
-  // the limbs of `a` are in the layout of the expert's code width
   if (bits == 4)
-    down_item<4>(a, blob, f, ent, nent, a.aq4, a.ae4);
+    down_item<4>(a, blob, f, ent, nent);
   else
-    down_item<2>(a, blob, f, ent, nent, a.aq2, a.ae2);
+    down_item<2>(a, blob, f, ent, nent);
 }
 
 // ---------------------------------------------------------------------------
@@ -378,7 +441,7 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 cudaError_t launch_topk(const TopkArgs& a, int B, cudaStream_t s) {
-  topk_kernel<<<B, kBlock, (size_t)a.E * sizeof(float), s>>>(a);
+  topk_kernel<<<B, 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t s) {

@@ -55,6 +55,9 @@ typedef enum {
 #define MOE_HAS_SHARED 1      /* the layer has one always-on shared expert */
 #define MOE_HAS_SHARED_GATE 2 /* the shared expert is scaled by sigmoid(shared_gate . xn) */
 #define MOE_NO_FUSED 4        /* moe_layer_decode: take the multi-kernel path even for B == 1 */
+#define MOE_PDL 8             /* moe_layer_decode, B == 1: programmatic dependent launch, so that the
+                                 kernel's weight prefetch overlaps the previous kernel on the stream
+                                 (instead of a cooperative launch; see moe_layer_decode) */
 
 /* Limits of this implementation (checked on entry). */
 #define MOE_MAX_TOPK 8

@@ -84,8 +84,38 @@ def test_device_generator_matches_host():
         assert np.array_equal(b.cpu().numpy().view(np.uint16), hb)
 
 
+def unpack_row_codes(packed, bits, ng):
+    """Canonical code bytes of one row from the packed order (host parser
+    written from the layout description, independent of the pack kernel).
+    4-bit: groups in chunks of up to 32; in a chunk of n groups, the first
+    16-byte halves of all n groups, then all second halves.
+    2-bit: field t of byte j of word m holds input 16m + (2j, 2j+1, 8+2j, 9+2j)[t]."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    if bits == 4:
+        out = np.empty(32 * ng, np.uint8)
+        for g in range(ng):
+            k, i = divmod(g, 32)
+            n = min(32, ng - 32 * k)
+            for h in range(2):
+                src = 1024 * k + 16 * (h * n + i)
+                out[32 * g + 16 * h:32 * g + 16 * h + 16] = packed[src:src + 16]
+        return out
+    nwords = packed.size // 4
+    vals = np.zeros(16 * nwords, np.int64)  # input index -> 2-bit code
+    for m in range(nwords):
+        w = int.from_bytes(packed[4 * m:4 * m + 4].tobytes(), "little")
+        for j in range(4):
+            for t, u in enumerate((2 * j, 2 * j + 1, 8 + 2 * j, 9 + 2 * j)):
+                vals[16 * m + u] = (w >> (8 * j + 2 * t)) & 3
+    canon = np.zeros(4 * nwords, np.uint8)
+    for c in range(16 * nwords):
+        canon[c // 4] |= np.uint8(vals[c] << (2 * (c % 4)))
+    return canon
+
+
 @pytest.mark.parametrize("bits", [4, 2])
-@pytest.mark.parametrize("shape", [TINY, dict(hidden=320, inter=64, n_experts=4, top_k=2)])
+@pytest.mark.parametrize("shape", [TINY, dict(hidden=320, inter=64, n_experts=4, top_k=2),
+                                   dict(hidden=3072, inter=128, n_experts=4, top_k=2)])
 def test_pack_layout_bit_exact(bits, shape):
     """Read the packed blob back with an independent host parser."""
     from tests.moe_testlib import pack_expert_device
@@ -104,19 +134,20 @@ def test_pack_layout_bit_exact(bits, shape):
     gu_codes, d_codes = H * bits // 8, I * bits // 8
     gu_row, d_row = pad16(gu_codes + 4 * (H // 64)), pad16(d_codes + 4 * (I // 64))
     assert n == I * 2 * gu_row + H * d_row
-    for r in range(I):
+    rows_to_check = sorted({0, 1, I // 2, I - 1})
+    for r in rows_to_check:
         for m, name in enumerate(("gate", "up")):
             row = blob[r * 2 * gu_row + m * gu_row:][:gu_row]
             c, s, b = canon[name]
-            assert np.array_equal(row[:gu_codes], c[r])
+            assert np.array_equal(unpack_row_codes(row[:gu_codes], bits, H // 64), c[r])
             sb = row[gu_codes:gu_codes + 4 * (H // 64)].view(np.uint16).reshape(-1, 2)
             assert np.array_equal(sb[:, 0], s[r]) and np.array_equal(sb[:, 1], b[r])
             assert np.all(row[gu_codes + 4 * (H // 64):] == 0)
     base = I * 2 * gu_row
     c, s, b = canon["down"]
-    for j in range(H):
+    for j in sorted({0, 1, H // 2, H - 1}):
         row = blob[base + j * d_row:][:d_row]
-        assert np.array_equal(row[:d_codes], c[j])
+        assert np.array_equal(unpack_row_codes(row[:d_codes], bits, I // 64), c[j])
         sb = row[d_codes:d_codes + 4 * (I // 64)].view(np.uint16).reshape(-1, 2)
         assert np.array_equal(sb[:, 0], s[j]) and np.array_equal(sb[:, 1], b[j])
         assert np.all(row[d_codes + 4 * (I // 64):] == 0)
@@ -191,21 +222,43 @@ def test_expert_forward_parity(bits, shape):
 
 
 # --------------------------------------------------------------------------- whole layer
-@pytest.mark.parametrize("path", ["fused", "multi"])
+PATH_FLAGS = {"fused": 0, "fused_pdl": M.MOE_PDL, "multi": M.MOE_NO_FUSED}
+
+
+@pytest.mark.parametrize("path", ["fused", "fused_pdl", "multi"])
 def test_layer_tiny(path):
     L = build_layer(D(TINY))
     h = G.hidden_states(G.SEED, 0, 6, 256)
     for t in range(6):
-        y, idx, w = decode(L, h[t:t + 1], flags_extra=M.MOE_NO_FUSED if path == "multi" else 0)
+        y, idx, w = decode(L, h[t:t + 1], flags_extra=PATH_FLAGS[path])
         check_token(L, h[t], y[0], idx[0], w[0])
 
 
-@pytest.mark.parametrize("path", ["fused", "multi"])
+@pytest.mark.parametrize("path", ["fused", "fused_pdl", "multi"])
 def test_layer_full_width(full4, path):
     h = G.hidden_states(G.SEED, 0, 3, 4096)
-    for t in range(3 if path == "fused" else 1):
-        y, idx, w = decode(full4, h[t:t + 1], flags_extra=M.MOE_NO_FUSED if path == "multi" else 0)
+    for t in range(3 if path != "multi" else 1):
+        y, idx, w = decode(full4, h[t:t + 1], flags_extra=PATH_FLAGS[path])
         check_token(full4, h[t], y[0], idx[0], w[0])
+
+
+def test_pdl_back_to_back_calls_match_oracle(full4):
+    """Many single-token calls queued back to back with programmatic dependent
+    launch, each call reading the h the previous call wrote (a chain), so that a
+    kernel that read h before the previous one finished would diverge."""
+    d = M.Dims(**{**full4.dims.__dict__, "flags": full4.dims.flags | M.MOE_PDL})
+    layer = M.make_layer(d, full4.experts, full4.stride, full4.router, shared=full4.shared, shared_bits=4)
+    h0 = G.hidden_states(G.SEED, 21, 1, 4096)
+    h = torch.from_numpy(h0.copy()).cuda()
+    ws = workspace(d, 1)
+    n = 6
+    for _ in range(n):
+        M.moe_layer_decode(layer, h, ws)
+    assert M.moe_get_device_status(ws) == 0
+    ref = h0[0].astype(np.float64)
+    for _ in range(n):
+        ref = full4.oracle(ref)["y"]
+    assert rel_err(h.cpu().numpy()[0], ref) <= REL_TOL
 
 
 def test_fused_is_deterministic(full4):
@@ -237,7 +290,7 @@ def test_layer_two_bit_full_width(B):
         check_token(L, h[t], y[t], idx[t], w[t])
 
 
-@pytest.mark.parametrize("path", ["fused", "multi"])
+@pytest.mark.parametrize("path", ["fused", "fused_pdl", "multi"])
 @pytest.mark.parametrize("variant", ["gamma_gate", "no_shared", "e_equals_k", "k1", "odd_shape", "stride_pad",
                                      "two_bit_tiny"])
 def test_layer_edge_cases(path, variant):
@@ -261,7 +314,22 @@ def test_layer_edge_cases(path, variant):
     L = build_layer(D(shape, **kw), **bkw)
     h = G.hidden_states(G.SEED, 4, 3, L.dims.hidden)
     for t in range(3):
-        y, idx, w = decode(L, h[t:t + 1], flags_extra=M.MOE_NO_FUSED if path == "multi" else 0)
+        y, idx, w = decode(L, h[t:t + 1], flags_extra=PATH_FLAGS[path])
+        check_token(L, h[t], y[0], idx[0], w[0])
+
+
+def test_workspace_reused_across_shapes():
+    """One workspace serves layers of different top-K and with and without a
+    shared expert, in turn: the grid barriers of the single-token kernel must
+    stay in step whichever subset a call uses."""
+    L4 = build_layer(D(TINY))
+    L2 = build_layer(D(TINY, top_k=2))
+    L0 = build_layer(D(TINY, flags=0))
+    big = M.Dims(**{**L4.dims.__dict__, "top_k": 8})
+    ws = workspace(big, 1)
+    h = G.hidden_states(G.SEED, 31, 6, 256)
+    for t, L in enumerate([L4, L2, L4, L0, L2, L4]):
+        y, idx, w = decode(L, h[t:t + 1], ws=ws)
         check_token(L, h[t], y[0], idx[0], w[0])
 
 
@@ -296,10 +364,10 @@ def test_nonfinite_input_sets_status():
 
 
 def test_barrier_timeout_is_reported_and_recoverable():
-    """A grid barrier that expects one block more than the grid never completes:
-    every block gives up after its bounded wait, the status word says TIMEOUT,
-    later launches return at once until the status is read, and then the
-    workspace works again."""
+    """Cross-block waits that expect a later launch's data never complete (the
+    workspace test hook): every block gives up after its bounded wait, the
+    status word says TIMEOUT, later launches return at once until the status
+    is read, and then the workspace works again."""
     L = build_layer(D(TINY))
     d = L.dims
     layer = L.c_layer()
