@@ -43,6 +43,8 @@ namespace {
 
 __device__ __forceinline__ int lo_row(int c, int P, int n) { return (int)((long long)c * n / P); }
 
+constexpr int kDnRows = 5;  // down rows per thread (the plan checks rows_d <= kDnRows * sets)
+
 // Limbs of one group of 64 values held four per lane by a half-warp (lane j of
 // the half holds values 4j .. 4j+3); all 32 lanes of the warp must call it.
 // Each lane assembles three of the group's limb words; when `store`, it writes
@@ -153,24 +155,41 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   int* const s_idx = reinterpret_cast<int*>(sm + a.plan.off_misc + 64);              // [kMaxTopK]
   float* const s_val = reinterpret_cast<float*>(sm + a.plan.off_misc + 96);          // [kMaxTopK]
   float* const s_coef = reinterpret_cast<float*>(sm + a.plan.off_misc + 128);        // [kMaxTopK + 1]
-  uint32_t* const s_mask = reinterpret_cast<uint32_t*>(sm + a.plan.off_misc + 168);  // issued, failed, epoch, hook
+  uint32_t* const s_mask = reinterpret_cast<uint32_t*>(sm + a.plan.off_misc + 168);  // issued, failed, epoch, hook, bumped, act
   const size_t gu_slot = a.plan.gu_slot, dn_slot = a.plan.dn_slot;
   const int part_stride = a.plan.part_stride;
   // mbarriers: [0] router rows, [1 + p] gate/up of expert p, [1 + NE + p] down
-  // of expert p, where expert p = 0 is the shared expert when present
+  // of expert p (expert p = 0 is the shared expert when present), then h and
+  // the published activations
+  const int bar_h = 1 + 2 * NE, bar_a = bar_h + 1, nbar = bar_h + 2;
+  float* const hbuf = reinterpret_cast<float*>(G + a.plan.off_hbuf);
+  const unsigned long long* const abuf = reinterpret_cast<const unsigned long long*>(G + a.plan.off_abuf);
 
-  // ---- prologue: barrier set-up, visible to every thread and to the copy
-  // engine before the first copy is issued
+  // ---- prologue.  Without PDL the caller's data can be read at once, so its
+  // loads go out first and overlap the barrier set-up and the first copies;
+  // with PDL the weight copies go first and the caller's data follows the
+  // dependency wait.
+  // Every block reads all of h, the logits and the activations; each comes in
+  // as one bulk copy per block (a few large requests), not as per-thread loads
+  // of the same lines by every block.
+  // Barrier set-up, visible to every thread and to the copy engine before the
+  // first copy is issued:
   if (tid == 0) {
-    for (int i = 0; i < 1 + 2 * NE; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < nbar; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
     fence_proxy_async();
     s_mask[0] = 0u;
     s_mask[1] = 0u;
+    s_mask[4] = 0u;  // counters this block has bumped (bit 0 logits, bit 1 activations)
   }
   __syncthreads();
   if (tid == 0) {
     uint32_t issued = 0u;
+    if (!kPDL) {
+      mbar_expect_tx(&bar[bar_h], (uint32_t)H * 4);
+      bulk_g2s(hbuf, a.h, (uint32_t)H * 4, &bar[bar_h]);
+      issued |= 1u << bar_h;
+    }
     if (nrr > 0) {
       mbar_expect_tx(&bar[0], (uint32_t)nrr * H * 2);
       uint8_t* rt = G + a.plan.off_rt;
@@ -197,6 +216,11 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   if (kPDL) {
     pdl_launch_dependents();
     pdl_wait_prior();
+    if (tid == 0) {
+      mbar_expect_tx(&bar[bar_h], (uint32_t)H * 4);
+      bulk_g2s(hbuf, a.h, (uint32_t)H * 4, &bar[bar_h]);
+      s_mask[0] |= 1u << bar_h;
+    }
   }
 
   // one warp waits on mbarrier i (one phase per launch); a give-up is recorded
@@ -208,14 +232,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   };
   auto failed = [&]() -> bool { return __syncthreads_or(tid == 0 && s_mask[1] != 0u) != 0; };
 
-  // ---- caller data and this launch's epoch, all in flight together
-  float4 hv0, hv1;
-  {
-    const float4* h4 = reinterpret_cast<const float4*>(a.h);
-    hv0 = 4 * tid < H ? h4[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
-    hv1 = 4 * (tid + kBlock) < H ? h4[tid + kBlock] : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  const float hres = tid < nj ? a.h[j0 + tid] : 0.f;
+  // ---- this launch's epoch
   if (tid == 0) {
     // every block of every launch adds one, so this launch is number count / P
     const unsigned long long n = atomicAdd(&a.hdr->launches, 1ull);
@@ -223,7 +240,12 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     s_mask[3] = *(volatile uint32_t*)&a.hdr->bar_extra;  // test hook: readers expect a later epoch
   }
   if (__syncthreads_or(tid == 0 && *(volatile uint32_t*)&a.hdr->abort)) goto cleanup;
+  warp_wait(bar_h);
   {
+    float4 hv0 = 4 * tid < H ? reinterpret_cast<const float4*>(hbuf)[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 hv1 =
+        4 * (tid + kBlock) < H ? reinterpret_cast<const float4*>(hbuf)[tid + kBlock] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float hres = tid < nj ? hbuf[j0 + tid] : 0.f;
     const uint32_t epoch = s_mask[2];           // written with every published word
     const uint32_t expect = epoch + s_mask[3];  // awaited by every reader
 
@@ -317,14 +339,21 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       }
     }
     if (failed()) goto cleanup;
-    if (tid < nrr) {
-      float v = 0.f;
+    if (wid == 0) {
+      if (lane < nrr) {
+        float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) v += rpart[tid * kWarps + w];
-      v *= rs;
-      const int e = tid < ne ? e0 + tid : E;  // the shared-gate logit is row E
-      if (e < E && a.offset) v += a.offset[e];
-      st_pub(a.pub_logits + e, v, epoch);
+        for (int w = 0; w < kWarps; ++w) v += rpart[lane * kWarps + w];
+        v *= rs;
+        const int e = lane < ne ? e0 + lane : E;  // the shared-gate logit is row E
+        if (e < E && a.offset) v += a.offset[e];
+        st_pub(a.pub_logits + e, v, epoch);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        red_relaxed_add_u64(&a.hdr->published_logits, 1ull);
+        s_mask[4] |= 1u;
+      }
     }
 
     // ---- shared expert gate/up (its rows were staged first)
@@ -343,11 +372,14 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       if (wid != 0) named_arrive(1, kBlock);
       if (wid == 0) {
         named_sync(1, kBlock);
-        bool ok = true, ready = true;
+        bool ok = true;
+        bool ready = lane != 0 || wait_count(a.hdr, &a.hdr->published_logits, (unsigned long long)P * expect);
+        ready = __all_sync(0xffffffffu, ready);
         uint32_t key[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) key[i] = 0u;
-        // published logits of this launch: lane l polls experts l, l + 32, ...
+        // logits of this launch: lane l reads experts l, l + 32, ... (all of
+        // its words in flight together; a word not yet visible is polled again)
         const int mine = E > lane ? (E - lane + 31) / 32 : 0;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
@@ -396,16 +428,6 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
                 issued |= 2u << (hs + k);
               }
             }
-            for (int k = 0; k < K; ++k) {
-              const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
-              if (nj > 0) {
-                const uint32_t bytes = (uint32_t)nj * r_d_row;
-                mbar_expect_tx(&bar[1 + NE + hs + k], bytes);
-                bulk_g2s(D + (size_t)(hs + k) * dn_slot, blob + r_d_off + (size_t)j0 * r_d_row, bytes,
-                         &bar[1 + NE + hs + k]);
-                issued |= 2u << (NE + hs + k);
-              }
-            }
             s_mask[0] = issued;
             chosen_softmax(s_val, K, s_coef + hs);
             if (hs) s_coef[0] = a.has_gate ? 1.0f / (1.0f + expf(-gate_logit)) : 1.0f;
@@ -428,7 +450,20 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       Limbs xl;
       float2 xe;
       load_x(xl, xe);
-      for (int k = 0; k < K; ++k) gate_up(hs + k, G + (size_t)k * gu_slot, a.bits, xl, xe);
+      for (int k = 0; k < K; ++k) {
+        gate_up(hs + k, G + (size_t)k * gu_slot, a.bits, xl, xe);
+        // routed down rows are needed last: warp 0 issues expert k's copy once
+        // its gate/up rows have landed (warp 0 has gate/up rows whenever the
+        // block has any, and gate_up waited for them), which keeps the copies
+        // in flight per SM few
+        if (wid == 0 && lane == 0 && nj > 0) {
+          const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
+          const uint32_t bytes = (uint32_t)nj * r_d_row;
+          mbar_expect_tx(&bar[1 + NE + hs + k], bytes);
+          bulk_g2s(D + (size_t)(hs + k) * dn_slot, blob + r_d_off + (size_t)j0 * r_d_row, bytes, &bar[1 + NE + hs + k]);
+          s_mask[0] |= 2u << (NE + hs + k);
+        }
+      }
     }
 
     // ---- SwiGLU of every expert's rows, weighted by the expert's routing
@@ -444,6 +479,27 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       }
       st_pub(a.pub_act + (size_t)p * I + r0 + i, s_coef[p] * silu_mul(rs * gsum, rs * usum), epoch);
     }
+    __syncthreads();
+    if (tid == 0) {
+      red_relaxed_add_u64(&a.hdr->published_act, 1ull);
+      s_mask[4] |= 2u;
+    }
+    // activation reader: one thread waits on the counter and copies every
+    // published activation into this block's gate/up area (its generic reads
+    // are complete: block barrier above), then every thread checks the epochs
+    // of the words it needs and polls a late word again
+    if (tid == 0) {
+      const bool ok = wait_count(a.hdr, &a.hdr->published_act, (unsigned long long)P * expect);
+      if (ok) {
+        fence_proxy_async();
+        mbar_expect_tx(&bar[bar_a], (uint32_t)a.plan.abuf_bytes);
+        bulk_g2s(G + a.plan.off_abuf, a.pub_act, (uint32_t)a.plan.abuf_bytes, &bar[bar_a]);
+        s_mask[0] |= 1u << bar_a;
+      }
+      s_mask[5] = ok ? 0u : 1u;
+    }
+    if (__syncthreads_or(tid == 0 && s_mask[5] != 0u)) goto cleanup;
+    warp_wait(bar_a);
 
     // ---- limbs of every weighted a: a half-warp per group, 2 groups per warp per pass
     {
@@ -454,8 +510,16 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         const bool real = gi < ngroups;
         const int gq = real ? gi : base;  // the idle half takes part in the shuffles
         const int p = gq / ngi, g = gq - p * ngi;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (ready) ready = poll_pub<4>(a.hdr, a.pub_act + (size_t)p * I + g * kGroup + 4 * (lane & 15), 1, 4, expect, v);
+        const size_t w0 = (size_t)p * I + g * kGroup + 4 * (lane & 15);
+        float v[4];
+        bool late = false;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const unsigned long long w = abuf[w0 + i];
+          late |= !pub_ready(w, expect);
+          v[i] = pub_value(w);
+        }
+        if (late && ready) ready = poll_pub<4>(a.hdr, a.pub_act + w0, 1, 4, expect, v);
         const bool f = quantize_group4(make_float4(v[0], v[1], v[2], v[3]), lane, real,
                                        AL + (size_t)p * ngi * kLimbBytes, ngi, g, AE + (size_t)p * ngi + g);
         fin &= f || !real;
@@ -481,10 +545,19 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         const float2 es = AE[(size_t)p * ngi + g];
         const uint8_t* base = D + (size_t)p * dn_slot;
         const bool b4 = (p < hs ? a.shared_bits : a.bits) == 4;
-        for (int r = set; r < nj; r += S) {
-          const float v = b4 ? row_group<4>(base + (size_t)r * f4.d_row, ngi, f4.d_codes, g, L, es)
-                             : row_group<2>(base + (size_t)r * f2.d_row, ngi, f2.d_codes, g, L, es);
-          pdn[r * Q + q] = v;
+        // up to kDnRows independent rows per thread, interleaved for ILP
+        if (b4) {
+#pragma unroll
+          for (int k = 0; k < kDnRows; ++k) {
+            const int r = set + k * S;
+            if (r < nj) pdn[r * Q + q] = row_group<4>(base + (size_t)r * f4.d_row, ngi, f4.d_codes, g, L, es);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kDnRows; ++k) {
+            const int r = set + k * S;
+            if (r < nj) pdn[r * Q + q] = row_group<2>(base + (size_t)r * f2.d_row, ngi, f2.d_codes, g, L, es);
+          }
         }
       }
       if (failed()) goto cleanup;
@@ -505,11 +578,14 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   return;
 
 cleanup:
-  // leave only after this block's own copies in flight have landed
+  // leave only after this block's own copies in flight have landed, and with
+  // every counter advanced by this block as in a complete launch
   __syncthreads();
   if (tid == 0) {
+    if (!(s_mask[4] & 1u)) red_relaxed_add_u64(&a.hdr->published_logits, 1ull);
+    if (!(s_mask[4] & 2u)) red_relaxed_add_u64(&a.hdr->published_act, 1ull);
     const uint32_t issued = s_mask[0];
-    for (int i = 0; i < 1 + 2 * NE; ++i)
+    for (int i = 0; i < nbar; ++i)
       if (issued >> i & 1u) mbar_wait(&bar[i], 0);
   }
   __syncthreads();
@@ -533,6 +609,10 @@ bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, i
   if (2 * p.rows_gu > 2 * (kWarps / mh.chunks) * mh.rpp) return false;
   if (p.rows_d > 2 * kWarps * mi.rpp) return false;
   if (p.rows_gu > 32 || p.rows_r > 32 || p.rows_d > kBlock / 16) return false;
+  {
+    const int Q = NE * fr.ng_i, S = Q > 0 ? kBlock / Q : 0;
+    if (S < 1 || p.rows_d > kDnRows * S) return false;
+  }
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -553,8 +633,12 @@ bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, i
   };
   p.off_sgu = sub(has_shared ? (size_t)p.rows_gu * fs.gu_pair : 0);
   p.off_rt = sub((size_t)p.rows_r * H * 2);
-  // after the gate/up phase the area also holds the down partials [rows_d][NE * ng_i]
-  p.off_g = take(std::max(std::max(pre, (size_t)K * p.gu_slot), (size_t)p.rows_d * NE * fr.ng_i * 4));
+  p.off_hbuf = sub((size_t)H * 4);  // h, one bulk copy
+  // after the gate/up phase: down partials, then the published activations
+  p.abuf_bytes = (size_t)NE * I * 8;
+  const size_t post = ((size_t)p.rows_d * NE * fr.ng_i * 4 + 127) / 128 * 128;
+  p.off_abuf = post;
+  p.off_g = take(std::max(std::max(pre, (size_t)K * p.gu_slot), post + p.abuf_bytes));
   // limbs: of x first (read into registers), later of every expert's activation
   const size_t ngroups = std::max((size_t)NE * fr.ng_i, (size_t)fr.ng_h);
   p.off_al = take(ngroups * kLimbBytes);
@@ -563,7 +647,7 @@ bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, i
   p.off_part = take((size_t)NE * p.part_stride * 4);
   p.off_rpart = take((size_t)p.rows_r * kWarps * 4);
   p.off_y = take((size_t)p.rows_d * 4);
-  p.off_bar = take((size_t)(1 + 2 * NE) * 8);
+  p.off_bar = take((size_t)(1 + 2 * NE + 2) * 8);
   p.off_misc = take(256);
   p.total = o + 128;  // slack for rounding the dynamic base up to 128 bytes
   if (p.total > (size_t)optin) return false;

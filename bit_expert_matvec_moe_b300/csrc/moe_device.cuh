@@ -72,7 +72,12 @@ struct WsHeader {
   // blocks of the single-token kernel that ever started: each launch adds its
   // grid size, so a block finds its launch's epoch as count / grid + 1
   unsigned long long launches;
-  uint32_t rsv3[6];
+  // blocks that finished publishing their logits / activations (each launch
+  // adds its grid size to each): a hint that lets one thread per block wait
+  // on a single word before the epoch-checked reads
+  unsigned long long published_logits;
+  unsigned long long published_act;
+  uint32_t rsv3[2];
 };
 static_assert(sizeof(WsHeader) == 64, "header size");
 constexpr size_t kHeaderErrorBytes = 32;
@@ -395,6 +400,26 @@ __device__ __forceinline__ unsigned long long ld_pub(const unsigned long long* p
 }
 __device__ __forceinline__ bool pub_ready(unsigned long long w, uint32_t epoch) { return (uint32_t)(w >> 32) == epoch; }
 __device__ __forceinline__ float pub_value(unsigned long long w) { return __uint_as_float((uint32_t)w); }
+
+__device__ __forceinline__ void red_relaxed_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// One thread: bounded wait (with back-off) until the counter reaches target;
+// false on timeout or when another block gave up.
+__device__ __forceinline__ bool wait_count(WsHeader* hdr, const unsigned long long* cnt, unsigned long long target) {
+  if ((long long)(ld_pub(cnt) - target) >= 0) return true;
+  const unsigned long long t0 = globaltimer();
+  while ((long long)(ld_pub(cnt) - target) < 0) {
+    if (*(volatile uint32_t*)&hdr->abort) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      atomicOr(&hdr->status, ST_TIMEOUT);
+      atomicExch(&hdr->abort, 1u);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
 
 // Bounded poll for n published words p[0], p[stride], ... (n <= 8) of this
 // epoch; the values go to out[].  On timeout, or when another block gave up,
