@@ -16,7 +16,8 @@ from ._native import MOE_HAS_SHARED, MOE_HAS_SHARED_GATE, MOE_NO_FUSED, MOE_PDL 
 
 __all__ = [
     "Dims", "MoeError", "moe_packed_expert_bytes", "moe_workspace_bytes", "moe_workspace_init",
-    "moe_pack_weights", "moe_route", "moe_expert_forward", "moe_layer_decode", "moe_get_device_status",
+    "moe_pack_weights", "moe_route", "moe_expert_forward", "moe_layer_decode", "moe_layer_decode_noalloc",
+    "moe_get_device_status",
     "make_layer",
 ]
 
@@ -121,6 +122,17 @@ def moe_layer_decode(layer: N.moe_layer, h, ws, logit_offset=None, idx_out=None,
     _check(N.load().moe_layer_decode(ctypes.byref(layer), _ptr(h), B, _ptr(logit_offset), _ptr(idx_out), _ptr(w_out),
                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_layer_decode")
+
+
+def moe_layer_decode_noalloc(layer: N.moe_layer, h, logit_offset=None, idx_out=None, w_out=None, status_out=None,
+                             stream=None) -> None:
+    """Single-token layer without a caller workspace (the library's fixed
+    device array instead; see include/moe.h).  h is [1, hidden]."""
+    if h.shape[0] != 1:
+        raise ValueError("moe_layer_decode_noalloc takes one token")
+    _check(N.load().moe_layer_decode_noalloc(ctypes.byref(layer), _ptr(h), _ptr(logit_offset), _ptr(idx_out),
+                                             _ptr(w_out), _ptr(status_out), _stream(stream)),
+           "moe_layer_decode_noalloc")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

@@ -28,6 +28,7 @@ EXPORTS = (
     "moe_route",
     "moe_expert_forward",
     "moe_layer_decode",
+    "moe_layer_decode_noalloc",
     "moe_get_device_status",
     "moe_status_string",
     "moe_last_error_message",
@@ -86,6 +87,8 @@ def load() -> ctypes.CDLL:
     lib.moe_expert_forward.argtypes = [P(moe_dims), I32, VP, VP, I32, VP, VP, I32, VP, SZ, VP]
     lib.moe_layer_decode.restype = ctypes.c_int
     lib.moe_layer_decode.argtypes = [P(moe_layer), VP, I32, VP, VP, VP, VP, SZ, VP]
+    lib.moe_layer_decode_noalloc.restype = ctypes.c_int
+    lib.moe_layer_decode_noalloc.argtypes = [P(moe_layer), VP, VP, VP, VP, VP, VP]
     lib.moe_get_device_status.restype = ctypes.c_int
     lib.moe_get_device_status.argtypes = [VP, VP]
     lib.moe_status_string.restype = ctypes.c_char_p

@@ -10,7 +10,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_decode_b1.cu"]
+SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_decode_b1.cu", "moe_noalloc.cu"]
 HEADERS = ["moe_device.cuh", "moe_internal.h"]
 LIB = os.path.join(HERE, "libmoe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

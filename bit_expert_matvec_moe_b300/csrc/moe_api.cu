@@ -86,6 +86,10 @@ int current_device() {
 
 }  // namespace
 
+namespace moe {
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_packed_expert_bytes(const moe_dims* dims, int32_t bits) {

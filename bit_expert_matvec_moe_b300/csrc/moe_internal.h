@@ -3,6 +3,7 @@
 
 #include <algorithm>
 #include <cstddef>
+#include <string>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -160,5 +161,8 @@ bool decode_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_
 bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, int shared_bits, int has_shared,
                      int has_gate, DecodePlan* out);
 cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s);
+
+// Text returned by moe_last_error_message() for this thread.
+void set_last_error(const std::string& msg);
 
 }  // namespace moe

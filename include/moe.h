@@ -198,6 +198,36 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B,
  */
 moe_status moe_get_device_status(void* ws, moe_stream_t stream);
 
+/*
+ * The single-token layer (as moe_layer_decode with B == 1) for callers that
+ * cannot allocate device memory.  This call has no counterpart on the
+ * Flash-MoE pages; it exists for callers that are given their input and
+ * output buffers but no way to allocate: code running inside another
+ * framework's memory pool, stream-ordered pipelines that forbid allocation on
+ * their hot path, and plugins that may not call cudaMalloc.  Instead of a
+ * caller workspace it uses a fixed array of MOE_NOALLOC_SCRATCH_BYTES of device
+ * memory owned by the library (a static __device__ symbol: every GPU that
+ * loads the library holds it until the process exits).  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   layer, h, logit_offset, idx_out, w_out   as in moe_layer_decode, B = 1
+ *   status_out   device int32 or NULL: receives this call's device status bits
+ *                (0 ok; 1 a bounded wait ran out, as MOE_ERR_TIMEOUT; 2 a
+ *                non-finite activation, as MOE_ERR_NONFINITE), copied on stream
+ * Returns MOE_ERR_UNSUPPORTED (text in moe_last_error_message) when the layer
+ * needs more scratch than the array holds ((experts + 1) + (top_k + 1) * inter
+ * eight-byte words plus a 256-byte header) or falls outside the single-token
+ * kernel (hidden <= 4096, inter <= 2048).
+ * The first call on a device looks up the array's address and clears it with a
+ * synchronous cudaMemset, so make that first call before any stream capture.
+ * Every call shares the one array and keeps its contents for the next call:
+ * calls that may overlap on the GPU (different streams, or graphs replayed
+ * concurrently) race and must be serialised by the caller.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (192u * 1024u)
+moe_status moe_layer_decode_noalloc(const moe_layer* layer, float* h, const float* logit_offset,
+                                    int32_t* idx_out, float* w_out, int32_t* status_out,
+                                    moe_stream_t stream);
+
 /* Static text of a status code. */
 const char* moe_status_string(moe_status s);
 

@@ -1,0 +1,79 @@
+"""moe_layer_decode_noalloc: the single-token layer for callers that cannot
+allocate device memory (they are handed their input and output buffers only,
+e.g. inside another framework's memory pool or an allocation-free hot path).
+It keeps its cross-block state in the library's fixed device array instead of
+a caller workspace.  Its output must match moe_layer_decode's on the same
+inputs, on consecutive calls (the array carries its state from call to call).
+This file is collected last, so a failure here comes after every other test."""
+import numpy as np
+import pytest
+
+from synth import generate as G
+from tests.moe_testlib import REL_TOL, build_layer, rel_err, workspace
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import bit_expert_matvec_moe_b300 as M  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from bit_expert_matvec_moe_b300 import build
+    from synth import device
+
+    build.build()
+    device.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _decode_with_workspace(L, h_np):
+    h = torch.from_numpy(h_np.copy()).cuda()
+    idx = torch.empty((1, L.dims.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((1, L.dims.top_k), dtype=torch.float32, device="cuda")
+    ws = workspace(L.dims, 1)
+    M.moe_layer_decode(L.c_layer(), h, ws, idx_out=idx, w_out=w)
+    assert M.moe_get_device_status(ws) == 0
+    return h.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def _decode_noalloc(L, h_np):
+    h = torch.from_numpy(h_np.copy()).cuda()
+    idx = torch.empty((1, L.dims.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((1, L.dims.top_k), dtype=torch.float32, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    M.moe_layer_decode_noalloc(L.c_layer(), h, idx_out=idx, w_out=w, status_out=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return h.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", [dict(hidden=256, inter=128, n_experts=16, top_k=4),
+                                   dict(hidden=4096, inter=1024, n_experts=64, top_k=4)])
+def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(shape):
+    L = build_layer(M.Dims(flags=M.MOE_HAS_SHARED, **shape), gen="device" if shape["hidden"] > 1024 else "host")
+    hs = G.hidden_states(G.SEED, 41, 2, shape["hidden"])
+    for t in range(2):  # two calls in a row on the shared array
+        y_ref, idx_ref, w_ref = _decode_with_workspace(L, hs[t:t + 1])
+        y, idx, w = _decode_noalloc(L, hs[t:t + 1])
+        assert np.array_equal(idx, idx_ref)
+        assert rel_err(w, w_ref) <= REL_TOL
+        assert rel_err(y[0], y_ref[0]) <= REL_TOL
+        assert rel_err(y[0] - hs[t], y_ref[0] - hs[t]) <= REL_TOL
+
+
+def test_noalloc_rejects_layers_beyond_its_array():
+    """A layer whose cross-block state exceeds the fixed array is refused with a
+    clear error before anything is enqueued."""
+    from bit_expert_matvec_moe_b300 import _native as N
+
+    d = M.Dims(hidden=4096, inter=4096, n_experts=1024, top_k=8, flags=M.MOE_HAS_SHARED)
+    stride = M.moe_packed_expert_bytes(d, 4)
+    fake = torch.empty(16, dtype=torch.uint8, device="cuda")
+    layer = M.make_layer(d, fake, stride, fake, shared=fake)
+    h = torch.zeros((1, 4096), dtype=torch.float32, device="cuda")
+    with pytest.raises(M.MoeError) as err:
+        M.moe_layer_decode_noalloc(layer, h)
+    assert err.value.status == N.MOE_ERR_UNSUPPORTED
+    assert "scratch array" in str(N.load().moe_last_error_message().decode())
