@@ -45,49 +45,77 @@ __device__ __forceinline__ int lo_row(int c, int P, int n) { return (int)((long 
 
 constexpr int kDnRows = 5;  // down rows per thread (the plan checks rows_d <= kDnRows * sets)
 
-// Limbs of one group of 64 values held four per lane by a half-warp (lane j of
-// the half holds values 4j .. 4j+3); all 32 lanes of the warp must call it.
-// Each lane assembles three of the group's limb words; when `store`, it writes
-// them (limb vector `vec` of ng groups, group g) and lane 0 of the half writes
-// the group factors to *es.  Returns false when a value is not finite.
-__device__ __forceinline__ bool quantize_group4(float4 x, int lane, bool store, uint8_t* vec, int ng, int g,
-                                                float2* es) {
+// Limbs of kG groups of 64 values, each held four per lane by a half-warp
+// (lane j of the half holds values 4j .. 4j+3 of its group); all 32 lanes of
+// the warp must call it.  The kG groups are independent, so their shuffle
+// chains interleave.  Each lane assembles three limb words per group; when
+// store[k], it writes them (limb vector vec[k] of ng groups, group g[k]) and
+// lane 0 of the half writes the group factors, times scale[k], to *es[k]
+// (scaling both factors scales the group's values).  Returns false when a
+// value is not finite.
+//
+// Per group: E is the exponent of the largest |value| (max = f * 2^E, f in
+// [0.5, 1)), read from its bits; every value becomes the integer
+// round(v * 2^(22 - E)) (|X| < 2^22), rounded to nearest-even by adding and
+// removing 1.5 * 2^23 in fp32, which is exact in that range.
+template <int kG>
+__device__ __forceinline__ bool quantize_groups(const float4 (&x)[kG], int lane, const bool (&store)[kG],
+                                                uint8_t* const (&vec)[kG], int ng, const int (&g)[kG],
+                                                float2* const (&es)[kG], const float (&scale)[kG]) {
   const int j = lane & 15;
-  float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+  float m[kG];
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const bool finite = isfinite(m);
-  int E = 0;
-  if (m > 0.f && finite) frexpf(m, &E);
-  E = max(E, -100);
-  const float up = __uint_as_float((uint32_t)(127 + 22 - E) << 23);  // 2^(22-E)
-  const float dn = __uint_as_float((uint32_t)(127 - 22 + E) << 23);  // 2^(E-22)
-  const int X0 = finite ? __float2int_rn(x.x * up) : 0;
-  const int X1 = finite ? __float2int_rn(x.y * up) : 0;
-  const int X2 = finite ? __float2int_rn(x.z * up) : 0;
-  const int X3 = finite ? __float2int_rn(x.w * up) : 0;
-  int s = X0 + X1 + X2 + X3;
+  for (int k = 0; k < kG; ++k) m[k] = fmaxf(fmaxf(fabsf(x[k].x), fabsf(x[k].y)), fmaxf(fabsf(x[k].z), fabsf(x[k].w)));
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+    for (int k = 0; k < kG; ++k) m[k] = fmaxf(m[k], __shfl_xor_sync(0xffffffffu, m[k], o));
+  }
+  bool finite_all = true;
+  int X[kG][4], s[kG];
+  float dn[kG];
+#pragma unroll
+  for (int k = 0; k < kG; ++k) {
+    const bool finite = isfinite(m[k]);
+    finite_all &= finite;
+    const int e = (int)((__float_as_uint(m[k]) >> 23) & 255u);
+    const int E = (m[k] > 0.f && finite) ? max(e - 126, -100) : 0;
+    const float up = __uint_as_float((uint32_t)(127 + 22 - E) << 23);  // 2^(22-E)
+    dn[k] = __uint_as_float((uint32_t)(127 - 22 + E) << 23);           // 2^(E-22)
+    const float v[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      X[k][i] = finite ? __float_as_int(fmaf(v[i], up, 12582912.0f)) - 0x4B400000 : 0;
+    s[k] = X[k][0] + X[k][1] + X[k][2] + X[k][3];
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+    for (int k = 0; k < kG; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], o);
+  }
   // word q = j >> 1 holds values 8q .. 8q+7; lane 2q has 8q..8q+3, lane 2q+1
   // has 8q+4..8q+7.  The even lane builds the "even" limb words (values 8q,
   // 8q+2, 8q+4, 8q+6), the odd lane the "odd" ones (8q+1, 8q+3, 8q+5, 8q+7).
   const bool odd = j & 1;
-  const int gotA = __shfl_xor_sync(0xffffffffu, odd ? X0 : X1, 1);
-  const int gotB = __shfl_xor_sync(0xffffffffu, odd ? X2 : X3, 1);
-  const int v0 = odd ? gotA : X0, v1 = odd ? gotB : X2, v2 = odd ? X1 : gotA, v3 = odd ? X3 : gotB;
-  if (store) {
-    const int q = j >> 1;
+  const int q = j >> 1;
 #pragma unroll
-    for (int l = 0; l < 3; ++l) {
-      const uint32_t word = ((uint32_t)(v0 >> (8 * l)) & 255u) | (((uint32_t)(v1 >> (8 * l)) & 255u) << 8) |
-                            (((uint32_t)(v2 >> (8 * l)) & 255u) << 16) | (((uint32_t)(v3 >> (8 * l)) & 255u) << 24);
-      const int w = 6 * q + 2 * l + (odd ? 1 : 0);
-      *reinterpret_cast<uint32_t*>(vec + ((size_t)(w >> 2) * ng + g) * 16 + (w & 3) * 4) = word;
+  for (int k = 0; k < kG; ++k) {
+    const int gotA = __shfl_xor_sync(0xffffffffu, odd ? X[k][0] : X[k][1], 1);
+    const int gotB = __shfl_xor_sync(0xffffffffu, odd ? X[k][2] : X[k][3], 1);
+    const int v0 = odd ? gotA : X[k][0], v1 = odd ? gotB : X[k][2], v2 = odd ? X[k][1] : gotA,
+              v3 = odd ? X[k][3] : gotB;
+    if (store[k]) {
+#pragma unroll
+      for (int l = 0; l < 3; ++l) {
+        const uint32_t word = ((uint32_t)(v0 >> (8 * l)) & 255u) | (((uint32_t)(v1 >> (8 * l)) & 255u) << 8) |
+                              (((uint32_t)(v2 >> (8 * l)) & 255u) << 16) | (((uint32_t)(v3 >> (8 * l)) & 255u) << 24);
+        const int w = 6 * q + 2 * l + (odd ? 1 : 0);
+        *reinterpret_cast<uint32_t*>(vec[k] + ((size_t)(w >> 2) * ng + g[k]) * 16 + (w & 3) * 4) = word;
+      }
+      if (j == 0) *es[k] = make_float2(dn[k] * scale[k], (float)s[k] * dn[k] * scale[k]);
     }
-    if (j == 0) *es = make_float2(dn, (float)s * dn);
   }
-  return finite;
+  return finite_all;
 }
 
 // Dot products of one lane's group with up to two rows of a slice in shared
@@ -251,22 +279,33 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
 
     // ---- x = h * gamma; sum of h^2; limbs of x.  Thread t holds values
     // 4t .. 4t+3 and 4(t+512) .. 4(t+512)+3, so warp w holds groups 2w, 2w+1
-    // of each pass; a pass is skipped by whole warps only.
+    // and 2w+16, 2w+17 (both passes quantised together).
     float ss = 0.f;
     bool finite = true;
+    {
+      float4 xs[2] = {hv0, hv1};
+      bool st[2];
+      int gs[2];
+      uint8_t* vs[2] = {AL, AL};
+      float2* es[2];
+      const float one[2] = {1.0f, 1.0f};
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i0 = 4 * (tid + kBlock * k);
-      float4 x = k == 0 ? hv0 : hv1;
-      ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, ss))));
-      if (a.gamma && i0 < H) {
-        const uint2 gw = *reinterpret_cast<const uint2*>(a.gamma + i0);
-        x.x *= bf16lo(gw.x); x.y *= bf16hi(gw.x); x.z *= bf16lo(gw.y); x.w *= bf16hi(gw.y);
+      for (int k = 0; k < 2; ++k) {
+        const int i0 = 4 * (tid + kBlock * k);
+        float4& x = xs[k];
+        ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, ss))));
+        if (a.gamma && i0 < H) {
+          const uint2 gw = *reinterpret_cast<const uint2*>(a.gamma + i0);
+          x.x *= bf16lo(gw.x); x.y *= bf16hi(gw.x); x.z *= bf16lo(gw.y); x.w *= bf16hi(gw.y);
+        }
+        st[k] = i0 < H;
+        gs[k] = st[k] ? i0 / kGroup : 0;
+        es[k] = AE + gs[k];
       }
-      if (k == 0) hv0 = x; else hv1 = x;
-      const int wbase = 4 * (32 * wid + kBlock * k);  // first value of this warp in this pass
-      if (wbase < H)
-        finite &= quantize_group4(x, lane, i0 < H, AL, ngh, i0 / kGroup, AE + i0 / kGroup);
+      hv0 = xs[0];
+      hv1 = xs[1];
+      if (4 * 32 * wid < H)  // the warp's first pass has values (whole warps skip)
+        finite = quantize_groups<2>(xs, lane, st, vs, ngh, gs, es, one);
     }
     ss = warp_sum(ss);
     if (lane == 0) s_red[wid] = ss;
@@ -501,28 +540,42 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     if (__syncthreads_or(tid == 0 && s_mask[5] != 0u)) goto cleanup;
     warp_wait(bar_a);
 
-    // ---- limbs of every weighted a: a half-warp per group, 2 groups per warp per pass
+    // ---- limbs of every weighted a: a half-warp per group, 2 groups per warp
+    // per pass, kActPasses passes quantised together
     {
+      constexpr int kActPasses = 3;
       bool fin = true, ready = true;
       const int ngroups = NE * ngi;
-      for (int base = 2 * wid; base < ngroups; base += 2 * kWarps) {
-        const int gi = base + (lane >> 4);
-        const bool real = gi < ngroups;
-        const int gq = real ? gi : base;  // the idle half takes part in the shuffles
-        const int p = gq / ngi, g = gq - p * ngi;
-        const size_t w0 = (size_t)p * I + g * kGroup + 4 * (lane & 15);
-        float v[4];
-        bool late = false;
+      for (int base0 = 2 * wid; base0 < ngroups; base0 += 2 * kWarps * kActPasses) {
+        float4 xs[kActPasses];
+        bool st[kActPasses];
+        int gs[kActPasses];
+        uint8_t* vs[kActPasses];
+        float2* es[kActPasses];
+        float one[kActPasses];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const unsigned long long w = abuf[w0 + i];
-          late |= !pub_ready(w, expect);
-          v[i] = pub_value(w);
+        for (int k = 0; k < kActPasses; ++k) {
+          const int gi = base0 + 2 * kWarps * k + (lane >> 4);
+          st[k] = gi < ngroups;
+          const int gq = st[k] ? gi : 0;  // an idle half takes part in the shuffles
+          const int p = gq / ngi, g = gq - p * ngi;
+          gs[k] = g;
+          vs[k] = AL + (size_t)p * ngi * kLimbBytes;
+          es[k] = AE + (size_t)p * ngi + g;
+          one[k] = 1.0f;
+          const size_t w0 = (size_t)p * I + g * kGroup + 4 * (lane & 15);
+          float v[4];
+          bool late = false;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const unsigned long long w = abuf[w0 + i];
+            late |= !pub_ready(w, expect);
+            v[i] = pub_value(w);
+          }
+          if (late && ready) ready = poll_pub<4>(a.hdr, a.pub_act + w0, 1, 4, expect, v);
+          xs[k] = make_float4(v[0], v[1], v[2], v[3]);
         }
-        if (late && ready) ready = poll_pub<4>(a.hdr, a.pub_act + w0, 1, 4, expect, v);
-        const bool f = quantize_group4(make_float4(v[0], v[1], v[2], v[3]), lane, real,
-                                       AL + (size_t)p * ngi * kLimbBytes, ngi, g, AE + (size_t)p * ngi + g);
-        fin &= f || !real;
+        fin &= quantize_groups<kActPasses>(xs, lane, st, vs, ngi, gs, es, one);
       }
       if (!ready) atomicOr(&s_mask[1], 1u);
       if (__syncthreads_or(!fin) && tid == 0) atomicOr(&a.hdr->status, ST_NONFINITE);
