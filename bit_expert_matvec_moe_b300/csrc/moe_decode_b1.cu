@@ -43,6 +43,12 @@ namespace {
 
 __device__ __forceinline__ int lo_row(int c, int P, int n) { return (int)((long long)c * n / P); }
 
+// Slot of activation value i in its expert's published vector: inside each
+// group of 64, value 4j + t goes to slot 16t + j, so that the half-warp that
+// reads a group (lane j takes values 4j .. 4j+3) reads 16 consecutive words per
+// load.
+__device__ __forceinline__ int act_slot(int i) { return (i & ~63) | ((i & 3) << 4) | ((i >> 2) & 15); }
+
 constexpr int kDnRows = 5;  // down rows per thread (the plan checks rows_d <= kDnRows * sets)
 
 // Limbs of kG groups of 64 values, each held four per lane by a half-warp
@@ -516,7 +522,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         gsum += pb[(2 * i) * mh.chunks + ch];
         usum += pb[(2 * i + 1) * mh.chunks + ch];
       }
-      st_pub(a.pub_act + (size_t)p * I + r0 + i, s_coef[p] * silu_mul(rs * gsum, rs * usum), epoch);
+      st_pub(a.pub_act + (size_t)p * I + act_slot(r0 + i), s_coef[p] * silu_mul(rs * gsum, rs * usum), epoch);
     }
     __syncthreads();
     if (tid == 0) {
@@ -563,16 +569,17 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
           vs[k] = AL + (size_t)p * ngi * kLimbBytes;
           es[k] = AE + (size_t)p * ngi + g;
           one[k] = 1.0f;
-          const size_t w0 = (size_t)p * I + g * kGroup + 4 * (lane & 15);
+          // values 4j .. 4j+3 of the group sit at slots j, j + 16, j + 32, j + 48
+          const size_t w0 = (size_t)p * I + g * kGroup + (lane & 15);
           float v[4];
           bool late = false;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const unsigned long long w = abuf[w0 + i];
+            const unsigned long long w = abuf[w0 + 16 * i];
             late |= !pub_ready(w, expect);
             v[i] = pub_value(w);
           }
-          if (late && ready) ready = poll_pub<4>(a.hdr, a.pub_act + w0, 1, 4, expect, v);
+          if (late && ready) ready = poll_pub<4>(a.hdr, a.pub_act + w0, 16, 4, expect, v);
           xs[k] = make_float4(v[0], v[1], v[2], v[3]);
         }
         fin &= quantize_groups<kActPasses>(xs, lane, st, vs, ngi, gs, es, one);
