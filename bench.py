@@ -33,6 +33,8 @@ sys.path.insert(0, ROOT)
 
 FULL = dict(hidden=4096, inter=1024, n_experts=512, top_k=4)
 TOKENS = 1000
+STACK_LAYERS = 40
+STACK_TOKENS = 256
 COPIES = 16
 FALLBACK_HBM_GBS = 6400.0
 
@@ -43,7 +45,8 @@ def parse():
     p.add_argument("--steps", type=int, default=5)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", type=int, default=2, choices=[2, 3, 4])
+    p.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
+                   help="2 full-width layer; 3 skewed routing (use --batch); 4 2-bit routed experts; 5 40-layer stack")
     p.add_argument("--batch", type=int, default=1)
     p.add_argument("--tokens", type=int, default=TOKENS)
     p.add_argument("--no-graph", action="store_true")
@@ -187,6 +190,11 @@ def run_ours(args, rank, world, local):
     T = args.tokens
     nsteps_tok = T // B
     layers = [M.make_layer(d, experts, stride, router[c], shared=shared[c], shared_bits=4) for c in range(COPIES)]
+    offsets = None
+    if args.config == 3:
+        # skewed routing: per-expert popularity offsets o_e ~ N(0, 1.5) added to every token's logits
+        o = torch.from_numpy(G.popularity_offsets(G.SEED, 0, d.n_experts)).cuda()
+        offsets = o.unsqueeze(0).expand(B, d.n_experts).contiguous()
     h_host = G.hidden_states(G.SEED, 100 + rank, T, d.hidden)
     h0 = torch.from_numpy(h_host).cuda()
     h = h0.clone()
@@ -199,7 +207,8 @@ def run_ours(args, rank, world, local):
     def one_step():
         for t in range(nsteps_tok):
             sl = slice(t * B, (t + 1) * B)
-            M.moe_layer_decode(layers[t % COPIES], h[sl], ws, idx_out=idx[sl], w_out=w[sl], stream=stream)
+            M.moe_layer_decode(layers[t % COPIES], h[sl], ws, logit_offset=offsets, idx_out=idx[sl], w_out=w[sl],
+                               stream=stream)
 
     # correctness smoke of the configuration (status word) before timing
     with torch.cuda.stream(stream):
@@ -268,14 +277,19 @@ def run_ours(args, rank, world, local):
                 e2e_ms.append(e0.elapsed_time(e1))
     e2e = float(np.mean(e2e_ms))
 
+    # unique routed experts per call (each streamed once for all of the call's tokens)
+    idx_h = idx[: nsteps_tok * B].cpu().numpy().reshape(nsteps_tok, B * d.top_k)
+    uniq = float(np.mean([len(np.unique(r)) for r in idx_h]))
+    T = nsteps_tok * B
     expert_bytes = d.top_k * M.moe_packed_expert_bytes(d, bits) + M.moe_packed_expert_bytes(d, 4)
+    call_bytes = uniq * M.moe_packed_expert_bytes(d, bits) + M.moe_packed_expert_bytes(d, 4)
     router_bytes = d.n_experts * d.hidden * 2
     launches_per_step = nsteps_tok
     per_launch_s = ms / 1e3 / launches_per_step
     tok_s = T * world / (ms / 1e3)
     peak, peak_kind = measured_hbm_peak()
-    alg = (expert_bytes + router_bytes) * B if B == 1 else None
-    achieved = (expert_bytes + router_bytes) / per_launch_s / 1e9 if B == 1 else None
+    alg = int(call_bytes + router_bytes)
+    achieved = (call_bytes + router_bytes) / per_launch_s / 1e9
     out = {
         "metric": "MoE layer decode tokens/s; expert-weight HBM GB/s vs ~8 TB/s peak",
         "value": round(tok_s, 1),
@@ -292,23 +306,25 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded SplitMix64; random-init weights of the stated shape)",
         "config": {
             "workload": (f"full-width single MoE layer, batch {B}: hidden 4096, {d.n_experts} experts, top-4 routed + 1 shared, "
-                         f"inter 1024, {bits}-bit group-64 affine quant, bf16 router, {T} decode tokens"),
+                         f"inter 1024, {bits}-bit group-64 affine quant, bf16 router, {T} decode tokens"
+                         + (", per-expert popularity offsets N(0, 1.5)" if offsets is not None else "")),
             "batch": B, "tokens_per_step": T, "launches_per_step": launches_per_step,
             "l2": f"inputs larger than L2 (3.6 GB routed experts); shared expert + router rotated over {COPIES} copies",
             "graph": graph is not None, "parallelism": f"replicas x{world}",
         },
-        "expert_gbs": round(expert_bytes * tok_s / world / 1e9, 1),
+        "expert_gbs": round(call_bytes / per_launch_s / 1e9, 1),
+        "unique_experts_per_call": round(uniq, 2),
         "us_per_token": round(ms * 1e3 / T, 3),
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode_b1_kernel",
+            "kernel": "decode_b1_kernel" if B == 1 else "gateup_kernel + down_kernel (batched path)",
             "achieved": round(achieved, 1) if achieved else None,
             "peak": peak,
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4) if achieved else None,
             "algorithmic_bytes_per_launch": alg,
-            "traffic": profiled_traffic("fused_decode_full_b1"),
+            "traffic": profiled_traffic("decode_b1_full_b1") if (B == 1 and bits == 4) else None,
         },
         "e2e": {"value": round(T * world / (e2e / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_pin.numel() * 4), "d2h_bytes_per_step": int(y_pin.numel() * 4 + idx_pin.numel() * 4)},
@@ -318,6 +334,148 @@ def run_ours(args, rank, world, local):
     print(f"# {tok_s:.1f} tokens/s, {ms * 1e3 / T:.3f} us/token, e2e {e2e:.3f} ms/step", file=sys.stderr, flush=True)
     if rank == 0 and args.config == 2 and B == 1 and args.cpu_seconds > 0:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- 40-layer stack
+def run_stack(args, rank, world, local):
+    """40 full-width 4-bit layers resident in HBM; each token passes all of them
+    (RMSNorm before, residual after each, inside every layer call).  Every layer
+    has its own copy of the 512-expert pool, shared expert and router (identical
+    bytes, distinct addresses: 145 GB of experts), so nothing a token reads is
+    left in L2 by the previous token.  Routing follows a reuse trace (token t's
+    slot j keeps token t-1's expert with probability 0.27), imposed through a
+    +30 logit offset on the traced experts, which leaves the routing weights
+    unchanged."""
+    import torch
+
+    import bit_expert_matvec_moe_b300 as M
+    from synth import generate as G
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    Lyr = STACK_LAYERS
+    T = args.tokens if args.tokens != TOKENS else STACK_TOKENS
+    d, experts0, stride, shared0, router0 = build_full_layer(torch, M, bits=4, copies=1, n_experts=args.experts)
+    if args.pdl:
+        d.flags |= M.MOE_PDL
+    E, K = d.n_experts, d.top_k
+    pools = [experts0] + [experts0.clone() for _ in range(Lyr - 1)]
+    shared = [shared0[0]] + [shared0[0].clone() for _ in range(Lyr - 1)]
+    routers = [router0[0]] + [router0[0].clone() for _ in range(Lyr - 1)]
+    layers = [M.make_layer(d, pools[l], stride, routers[l], shared=shared[l], shared_bits=4) for l in range(Lyr)]
+    trace = np.stack([G.reuse_trace(G.SEED, l, T, E, K) for l in range(Lyr)])  # [L, T, K]
+    offs_h = np.zeros((Lyr, T, E), dtype=np.float32)
+    for l in range(Lyr):
+        for t in range(T):
+            offs_h[l, t] = G.trace_offsets(trace[l, t], E)
+    offs = torch.from_numpy(offs_h).cuda()
+    h_host = G.hidden_states(G.SEED, 100 + rank, T, d.hidden)
+    h0 = torch.from_numpy(h_host).cuda()
+    h = h0.clone()
+    ws = torch.empty(M.moe_workspace_bytes(d, 1), dtype=torch.uint8, device="cuda")
+    M.moe_workspace_init(ws)
+    idx = torch.empty((Lyr, T, K), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def one_step():
+        for t in range(T):
+            for l in range(Lyr):
+                M.moe_layer_decode(layers[l], h[t:t + 1], ws, logit_offset=offs[l, t:t + 1], idx_out=idx[l, t:t + 1],
+                                   stream=stream)
+
+    with torch.cuda.stream(stream):
+        one_step()
+    assert M.moe_get_device_status(ws, stream) == 0
+    got = np.sort(idx.cpu().numpy(), axis=-1)
+    assert np.array_equal(got, np.sort(trace, axis=-1)), "routing does not follow the imposed trace"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        one_step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            h.copy_(h0)
+            graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    step_ms = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            h.copy_(h0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            e1.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    assert M.moe_get_device_status(ws, stream) == 0
+    ms = float(np.mean(step_ms))
+    # end to end: H2D of the step's hidden states, the 40-layer pass of every token, D2H of the outputs
+    h_pin = torch.from_numpy(h_host).pin_memory()
+    y_pin = torch.empty_like(h_pin).pin_memory()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for it in range(args.warmup + args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            h.copy_(h_pin, non_blocking=True)
+            graph.replay()
+            y_pin.copy_(h, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+    e2e = float(np.mean(e2e_ms))
+    layer_bytes = (K + 1) * M.moe_packed_expert_bytes(d, 4) + E * d.hidden * 2
+    tok_s = T * world / (ms / 1e3)
+    per_launch_s = ms / 1e3 / (T * Lyr)
+    peak, peak_kind = measured_hbm_peak()
+    achieved = layer_bytes / per_launch_s / 1e9
+    out = {
+        "metric": "MoE layer decode tokens/s; expert-weight HBM GB/s vs ~8 TB/s peak",
+        "value": round(tok_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u4 codes x fp32 activations (int32 dp4a group sums, fp32 accumulate)",
+        "data": "synthetic (seeded SplitMix64; random-init weights of the stated shape)",
+        "config": {
+            "workload": (f"{Lyr}-layer MoE decode stack resident in HBM: full-width 4-bit layers (hidden 4096, {E} experts, "
+                         f"top-4 + 1 shared, inter 1024), {T} tokens, top-4 reuse trace p=0.27"),
+            "batch": 1, "tokens_per_step": T, "layers": Lyr, "launches_per_step": T * Lyr,
+            "l2": "no reuse: every layer has its own expert pool, shared expert and router (145 GB of experts)",
+            "graph": True, "parallelism": f"replicas x{world}",
+        },
+        "expert_gbs": round((K + 1) * M.moe_packed_expert_bytes(d, 4) / per_launch_s / 1e9, 1),
+        "us_per_layer": round(per_launch_s * 1e6, 3),
+        "bytes_per_token": int(layer_bytes * Lyr),
+        "roofline": {
+            "bound": "hbm", "kernel": "decode_b1_kernel", "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "algorithmic_bytes_per_launch": int(layer_bytes), "traffic": None,
+        },
+        "e2e": {"value": round(T * world / (e2e / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_pin.numel() * 4), "d2h_bytes_per_step": int(y_pin.numel() * 4)},
+        "gpu_launches": T * Lyr * args.steps,
+        "clocks": ck,
+    }
+    print(f"# {tok_s:.1f} tokens/s through {Lyr} layers, {per_launch_s * 1e6:.3f} us/layer", file=sys.stderr, flush=True)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -413,6 +571,9 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.config == 5:
+        run_stack(args, rank, world, local)
         return
     run_ours(args, rank, world, local)
 

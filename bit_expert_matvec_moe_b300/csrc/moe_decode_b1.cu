@@ -199,10 +199,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   float* const hbuf = reinterpret_cast<float*>(G + a.plan.off_hbuf);
   const unsigned long long* const abuf = reinterpret_cast<const unsigned long long*>(G + a.plan.off_abuf);
 
-  // ---- prologue.  Without PDL the caller's data can be read at once, so its
-  // loads go out first and overlap the barrier set-up and the first copies;
-  // with PDL the weight copies go first and the caller's data follows the
-  // dependency wait.
+  // ---- prologue.
   // Every block reads all of h, the logits and the activations; each comes in
   // as one bulk copy per block (a few large requests), not as per-thread loads
   // of the same lines by every block.
@@ -217,44 +214,45 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     s_mask[4] = 0u;  // counters this block has bumped (bit 0 logits, bit 1 activations)
   }
   __syncthreads();
-  if (tid == 0) {
+  // copies of the prologue: bit 0 router rows, bit 1 shared gate/up rows, bit 2
+  // shared down rows.  Without PDL h goes first, then the rest in the order they
+  // are needed.  With PDL the shared expert's rows (needed last) go out before
+  // the dependency wait, and h and the router rows (needed first) right after
+  // it, so that they do not queue behind the shared rows.
+  auto issue = [&](uint32_t which) {
     uint32_t issued = 0u;
-    if (!kPDL) {
-      mbar_expect_tx(&bar[bar_h], (uint32_t)H * 4);
-      bulk_g2s(hbuf, a.h, (uint32_t)H * 4, &bar[bar_h]);
-      issued |= 1u << bar_h;
-    }
-    if (nrr > 0) {
+    if ((which & 1u) && nrr > 0) {
       mbar_expect_tx(&bar[0], (uint32_t)nrr * H * 2);
       uint8_t* rt = G + a.plan.off_rt;
       if (ne > 0) bulk_g2s(rt, a.router + (size_t)e0 * H, (uint32_t)ne * H * 2, &bar[0]);
       if (nrr > ne) bulk_g2s(rt + (size_t)ne * H * 2, a.gate, (uint32_t)H * 2, &bar[0]);
       issued |= 1u;
     }
-    if (hs) {
-      if (nr > 0) {
-        const uint32_t bytes = (uint32_t)nr * s_gu_pair;
-        mbar_expect_tx(&bar[1], bytes);
-        bulk_g2s(G + a.plan.off_sgu, a.shared + (size_t)r0 * s_gu_pair, bytes, &bar[1]);
-        issued |= 2u;
-      }
-      if (nj > 0) {
-        const uint32_t bytes = (uint32_t)nj * s_d_row;
-        mbar_expect_tx(&bar[1 + NE], bytes);
-        bulk_g2s(D, a.shared + s_d_off + (size_t)j0 * s_d_row, bytes, &bar[1 + NE]);
-        issued |= 2u << NE;
-      }
+    if ((which & 2u) && hs && nr > 0) {
+      const uint32_t bytes = (uint32_t)nr * s_gu_pair;
+      mbar_expect_tx(&bar[1], bytes);
+      bulk_g2s(G + a.plan.off_sgu, a.shared + (size_t)r0 * s_gu_pair, bytes, &bar[1]);
+      issued |= 2u;
     }
-    s_mask[0] = issued;
-  }
+    if ((which & 4u) && hs && nj > 0) {
+      const uint32_t bytes = (uint32_t)nj * s_d_row;
+      mbar_expect_tx(&bar[1 + NE], bytes);
+      bulk_g2s(D, a.shared + s_d_off + (size_t)j0 * s_d_row, bytes, &bar[1 + NE]);
+      issued |= 2u << NE;
+    }
+    return issued;
+  };
+  auto issue_h = [&]() {
+    mbar_expect_tx(&bar[bar_h], (uint32_t)H * 4);
+    bulk_g2s(hbuf, a.h, (uint32_t)H * 4, &bar[bar_h]);
+    return 1u << bar_h;
+  };
+  constexpr uint32_t kEarly = 6u;
+  if (tid == 0) s_mask[0] = kPDL ? issue(kEarly) : (issue_h() | issue(7u));
   if (kPDL) {
     pdl_launch_dependents();
     pdl_wait_prior();
-    if (tid == 0) {
-      mbar_expect_tx(&bar[bar_h], (uint32_t)H * 4);
-      bulk_g2s(hbuf, a.h, (uint32_t)H * 4, &bar[bar_h]);
-      s_mask[0] |= 1u << bar_h;
-    }
+    if (tid == 0) s_mask[0] |= issue_h() | issue(7u & ~kEarly);
   }
 
   // one warp waits on mbarrier i (one phase per launch); a give-up is recorded
