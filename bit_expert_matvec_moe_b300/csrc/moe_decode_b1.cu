@@ -257,8 +257,8 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
 
   // one warp waits on mbarrier i (one phase per launch); a give-up is recorded
   // and acted on at the next block barrier, so that all threads leave together
-  auto warp_wait = [&](int i) -> bool {
-    const bool ok = mbar_wait(&bar[i], 0);
+  auto warp_wait = [&](int i) -> bool {  // none once the block has failed
+    const bool ok = *(volatile uint32_t*)&s_mask[1] == 0u && mbar_wait(&bar[i], 0);
     if (!ok && lane == 0) atomicOr(&s_mask[1], 1u);
     return __all_sync(0xffffffffu, ok);
   };
@@ -499,7 +499,9 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         // its gate/up rows have landed (warp 0 has gate/up rows whenever the
         // block has any, and gate_up waited for them), which keeps the copies
         // in flight per SM few
-        if (wid == 0 && lane == 0 && nj > 0) {
+        // (only if routing succeeded: s_idx is written by top-K; this thread
+        // raised the failure flag itself when it did not)
+        if (wid == 0 && lane == 0 && nj > 0 && *(volatile uint32_t*)&s_mask[1] == 0u) {
           const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
           const uint32_t bytes = (uint32_t)nj * r_d_row;
           mbar_expect_tx(&bar[1 + NE + hs + k], bytes);

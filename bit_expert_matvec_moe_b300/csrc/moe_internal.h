@@ -13,8 +13,6 @@ namespace moe {
 
 constexpr int kBlock = 512;   // threads per block of the matvec kernels
 constexpr int kWarps = kBlock / 32;
-constexpr int kRowsGU = 8;    // gate/up row pairs per block (multi-kernel path)
-constexpr int kRowsD = 32;    // down rows per block (multi-kernel path)
 
 
 struct PackArgs {

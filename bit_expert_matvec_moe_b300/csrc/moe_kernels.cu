@@ -117,41 +117,64 @@ __global__ void __launch_bounds__(kBlock) norm_quant_kernel(NormQuantArgs a) {
 // router matvec: logits[b][e] = router[e] . xn[b] (+ offset[b][e]); row E is the
 // shared-expert gate vector when present (no offset)
 // ---------------------------------------------------------------------------
-// One warp per router row, tokens in register tiles of 8.  Lane l reads bf16
-// elements [8l + 256 s, 8l + 256 s + 8) at step s; partial sums are combined by
-// a fixed butterfly, so results do not depend on scheduling.
+// Tiled over (router rows, tokens): a block computes kRtRows rows x kRtTok
+// tokens, staging chunks of kRtK inputs of the rows (bf16) and of the tokens'
+// xn (fp32) in shared memory (rows padded by one word, so that the threads of
+// a warp, which read different rows or tokens at the same input, hit different
+// banks).  Thread t owns row t / 8 and tokens t % 8, t % 8 + 8; each output is
+// a fixed-order sum (four interleaved partial sums per chunk, added pairwise,
+// then chunk by chunk), so results do not depend on scheduling and rounding
+// chains stay short.
+constexpr int kRtRows = 32, kRtTok = 16, kRtK = 256;
 __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  __shared__ float xs[kRtTok][kRtK + 1];
+  __shared__ uint32_t rs[kRtRows][kRtK / 2 + 1];  // bf16 pairs
+  const int tid = threadIdx.x;
   const int nrows = a.E + (a.gate ? 1 : 0);
-  if (row >= nrows) return;
-  const uint16_t* R = row < a.E ? a.router + (size_t)row * a.H : a.gate;
-  for (int b0 = 0; b0 < a.B; b0 += 8) {
-    float acc[8];
+  const int row0 = blockIdx.x * kRtRows, b0 = blockIdx.y * kRtTok;
+  const int lr = tid >> 3, lt = tid & 7;
+  float acc0 = 0.f, acc1 = 0.f;
+  for (int k0 = 0; k0 < a.H; k0 += kRtK) {
+    const int kn = min(kRtK, a.H - k0);  // a multiple of 64
+    for (int i = tid; i < kRtTok * (kn / 4); i += 256) {
+      const int t = i / (kn / 4), c = 4 * (i - t * (kn / 4));
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b0 + t < a.B) v = *reinterpret_cast<const float4*>(a.xn + (size_t)(b0 + t) * a.H + k0 + c);
+      xs[t][c] = v.x; xs[t][c + 1] = v.y; xs[t][c + 2] = v.z; xs[t][c + 3] = v.w;
+    }
+    for (int i = tid; i < kRtRows * (kn / 8); i += 256) {
+      const int r = i / (kn / 8), c = 8 * (i - r * (kn / 8));
+      const int row = row0 + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (row < nrows) {
+        const uint16_t* R = row < a.E ? a.router + (size_t)row * a.H : a.gate;
+        v = *reinterpret_cast<const uint4*>(R + k0 + c);
+      }
+      rs[r][c / 2] = v.x; rs[r][c / 2 + 1] = v.y; rs[r][c / 2 + 2] = v.z; rs[r][c / 2 + 3] = v.w;
+    }
+    __syncthreads();
+    // four interleaved partial sums per chunk, added pairwise: short rounding chains
+    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < kn / 2; c += 4) {
 #pragma unroll
-    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
-    for (int c = 8 * lane; c < a.H; c += 256) {
-      const uint4 rw = *reinterpret_cast<const uint4*>(R + c);
-      const float r[8] = {bf16lo(rw.x), bf16hi(rw.x), bf16lo(rw.y), bf16hi(rw.y),
-                          bf16lo(rw.z), bf16hi(rw.z), bf16lo(rw.w), bf16hi(rw.w)};
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        if (b0 + t < a.B) {
-          const float4* x4 = reinterpret_cast<const float4*>(a.xn + (size_t)(b0 + t) * a.H + c);
-          const float4 xa = x4[0], xb = x4[1];
-          float s = acc[t];
-          s = fmaf(r[0], xa.x, s); s = fmaf(r[1], xa.y, s); s = fmaf(r[2], xa.z, s); s = fmaf(r[3], xa.w, s);
-          s = fmaf(r[4], xb.x, s); s = fmaf(r[5], xb.y, s); s = fmaf(r[6], xb.z, s); s = fmaf(r[7], xb.w, s);
-          acc[t] = s;
-        }
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w = rs[lr][c + q];
+        const float r0 = bf16lo(w), r1 = bf16hi(w);
+        p0[q] = fmaf(r1, xs[lt][2 * (c + q) + 1], fmaf(r0, xs[lt][2 * (c + q)], p0[q]));
+        p1[q] = fmaf(r1, xs[lt + 8][2 * (c + q) + 1], fmaf(r0, xs[lt + 8][2 * (c + q)], p1[q]));
       }
     }
+    acc0 += (p0[0] + p0[1]) + (p0[2] + p0[3]);
+    acc1 += (p1[0] + p1[1]) + (p1[2] + p1[3]);
+    __syncthreads();
+  }
+  const int row = row0 + lr;
+  if (row < nrows) {
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const float s = warp_sum(acc[t]);
-      const int b = b0 + t;
-      if (lane == 0 && b < a.B) {
-        float v = s;
+    for (int j = 0; j < 2; ++j) {
+      const int b = b0 + lt + 8 * j;
+      if (b < a.B) {
+        float v = j == 0 ? acc0 : acc1;
         if (row < a.E && a.offset) v += a.offset[(size_t)b * a.E + row];
         a.logits[(size_t)b * (a.E + 1) + row] = v;
       }
@@ -247,77 +270,144 @@ __global__ void __launch_bounds__(kBlock) bucket_kernel(BucketArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// dot products of `nrows` quantised rows with one activation vector
+// weight-stationary grouped matvecs (B > 1)
 // ---------------------------------------------------------------------------
-//   rows      row r starts at rows + row_off(r) (codes, then one (s,b) word per group)
-//   xq, xe    the vector's limbs (ng groups, layout of moe_device.cuh) and factors
-//   part      out: part[r * chunks + chunk] = partial dot over the chunk's groups
-// All warps of the block take part; the caller syncs after.
-template <int BITS, typename RowOff>
-__device__ __forceinline__ void rows_dot(const uint8_t* rows, RowOff row_off, int nrows, int ng, int codes_bytes,
-                                         const uint8_t* xq, const float2* xe, float* part, int wi, int nw, int lane) {
+// A block stages a tile of one expert's rows in shared memory once (cp.async),
+// then applies every token routed to that expert.  Lane g of a warp owns group
+// g of its row chunk: it loads the token's limbs of that group once (registers)
+// and runs them against each of the warp's rows of the tile (codes from shared
+// memory, conflict-free 16-byte loads in the packed layout); the lanes of a row
+// are reduced by shuffles.  Tokens go kTok at a time between block barriers;
+// per-row partials (one per row chunk) are summed in a fixed order, so results
+// are deterministic.  grid = (row tiles, work items); item u is expert
+// uniq_e[u] (or the shared expert) with its token entries; without a list
+// (single-expert mode) the item is `blob` with tokens 0..B-1.
+constexpr int kWsThreads = 256;
+constexpr int kWsWarps = kWsThreads / 32;
+constexpr int kGuTile = 32;   // gate/up rows per tile at most (16 pairs)
+constexpr int kDnTile = 128;  // down rows per tile at most
+constexpr int kTok = 8;       // tokens between block barriers
+constexpr int kMaxRowsPerLane = 8;
+
+// rows of a tile: what the warps' lane streams cover with kMaxRowsPerLane rows
+// per lane (rows of ng groups), capped; gate/up tiles hold whole row pairs
+__host__ __device__ inline int tile_cover(int ng) {
   const RowMap m = make_rowmap(ng);
-  const int chunk = wi % m.chunks;
-  const int stream = wi / m.chunks;
-  const int nstreams = nw / m.chunks;
-  if (stream >= nstreams) return;
-  const int sub = lane % m.lpr, slot = lane / m.lpr;
-  const int g = chunk * 32 + sub;
-  const bool gact = g < ng;
-  Limbs L;
-  float2 es = make_float2(0.f, 0.f);
-  if (gact) {
-    load_limbs(xq, ng, g, L);
-    es = xe[g];
-  } else {
-    zero_limbs(L);
-  }
-  const int step = nstreams * m.rpp;
-  for (int base = stream * m.rpp; base < nrows; base += step) {
-    const int r = base + slot;
-    float v = 0.f;
-    if (gact && r < nrows) v = row_group<BITS>(rows + row_off(r), ng, codes_bytes, g, L, es);
-    v = row_reduce(v, m.lpr);
-    if (sub == 0 && r < nrows) part[r * m.chunks + chunk] = v;
-  }
+  return kMaxRowsPerLane * (kWsWarps / m.chunks) * m.rpp;
+}
+__host__ __device__ inline int gu_tile_rows(int H) { return min(kGuTile, tile_cover(H / kGroup)) & ~1; }
+__host__ __device__ inline int dn_tile_rows(int I) { return min(kDnTile, tile_cover(I / kGroup)); }
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// grouped gate/up + SwiGLU: a[b][slot][r] = silu(Wg_r . xn_b) * (Wu_r . xn_b)
-// ---------------------------------------------------------------------------
-// grid = (row blocks of kRowsGU gate/up row pairs, work items); block = kBlock.
-// Item u is expert uniq_e[u] (or the shared expert) with its token entries.
-// Without a list (single-expert mode) the item is `blob` with tokens 0..B-1.
-template <int BITS>
-__device__ void gateup_item(const GateUpArgs& a, const uint8_t* blob, const Fmt& f, const int* ent, int nent) {
-  __shared__ float part[2 * kRowsGU * 4];  // up to 4 chunks (hidden <= 8192)
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int r0 = blockIdx.x * kRowsGU;
-  const int nr = min(kRowsGU, f.I - r0);
-  if (nr <= 0) return;
-  const RowMap m = make_rowmap(f.ng_h);
-  const uint8_t* rows = blob + (size_t)r0 * f.gu_pair;
-  auto off = [&](int r) { return (size_t)(r >> 1) * f.gu_pair + (size_t)(r & 1) * f.gu_row; };
-  for (int t = 0; t < nent; ++t) {
-    const int e = ent ? ent[t] : t * a.nslots;  // b * nslots + slot
-    const int b = e / a.nslots;
-    rows_dot<BITS>(rows, off, 2 * nr, f.ng_h, f.gu_codes, a.xq + (size_t)b * f.ng_h * kLimbBytes,
-                   a.xe + (size_t)b * f.ng_h, part, wid, nw, lane);
-    __syncthreads();
-    if ((int)threadIdx.x < nr) {
-      const int r = threadIdx.x;
-      float g = 0.f, u = 0.f;
-      for (int c = 0; c < m.chunks; ++c) {
-        g += part[(2 * r) * m.chunks + c];
-        u += part[(2 * r + 1) * m.chunks + c];
+// rows [0, nrows) (row r at src(r), row_bytes each, a multiple of 16) to dst + r * row_bytes
+template <typename Src>
+__device__ __forceinline__ void stage_rows(uint8_t* dst, Src src, int nrows, int row_bytes) {
+  const int chunks = row_bytes / 16;
+  for (int i = threadIdx.x; i < nrows * chunks; i += blockDim.x) {
+    const int r = i / chunks, c = i - r * chunks;
+    cp_async16(dst + (size_t)r * row_bytes + 16 * c, src(r) + 16 * c);
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+}
+
+// partial dots of one token with the warp's rows of a staged tile: rows
+// r_first + k * r_step (k < kRows, those < nrows), row r at tile + r * row_bytes;
+// out[k] = the row's sum over this lane's chunk of groups (same on all lanes of
+// the row).  All lanes of the warp call it.
+template <int BITS, int kRows>
+__device__ __forceinline__ void tile_rows(const uint8_t* tile, int row_bytes, int codes_bytes, int ng, int g,
+                                          bool gact, const Limbs& L, float2 es, int r_first, int r_step, int nrows,
+                                          int lpr, float (&out)[kRows]) {
+  float v[kRows];
+#pragma unroll
+  for (int k = 0; k < kRows; ++k) {
+    const int r = r_first + k * r_step;
+    v[k] = (gact && r < nrows) ? row_group<BITS>(tile + (size_t)r * row_bytes, ng, codes_bytes, g, L, es) : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < kRows; ++k) out[k] = row_reduce(v[k], lpr);
+}
+
+// One work item's tile: rows [0, nrows) of the tile staged; per token chunk,
+// warp w takes chunk w % chunks of the groups and rows (w / chunks) * rpp + ...;
+// the partials go to part[t][r][chunk] and finish(t0, ntok) combines them.
+template <int BITS, int kRows, typename Vec, typename Finish>
+__device__ __forceinline__ void tile_tokens(const uint8_t* tile, int row_bytes, int codes_bytes, int ng, int nrows,
+                                            int nent, Vec vec_of, float* part, Finish finish) {
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const RowMap m = make_rowmap(ng);
+  const int chunk = wi % m.chunks, nstreams = kWsWarps / m.chunks;
+  const int g = chunk * 32 + lane % m.lpr;
+  const bool gact = g < ng && wi < nstreams * m.chunks;
+  const int r_first = (wi / m.chunks) * m.rpp + lane / m.lpr, r_step = nstreams * m.rpp;
+  for (int t0 = 0; t0 < nent; t0 += kTok) {
+    const int ntok = min(kTok, nent - t0);
+    for (int t = 0; t < ntok; ++t) {
+      const uint8_t* q;
+      const float2* e;
+      vec_of(t0 + t, q, e);
+      Limbs L;
+      float2 es = make_float2(0.f, 0.f);
+      if (gact) {
+        load_limbs(q, ng, g, L);
+        es = e[g];
+      } else {
+        zero_limbs(L);
       }
-      a.a_out[(size_t)e * f.I + r0 + r] = silu_mul(g, u);
+      float o[kRows];
+      tile_rows<BITS, kRows>(tile, row_bytes, codes_bytes, ng, g, gact, L, es, r_first, r_step, nrows, m.lpr, o);
+      if (lane % m.lpr == 0 && gact) {
+#pragma unroll
+        for (int k = 0; k < kRows; ++k) {
+          const int r = r_first + k * r_step;
+          if (r < nrows) part[(t * nrows + r) * m.chunks + chunk] = o[k];
+        }
+      }
     }
     __syncthreads();
+    finish(t0, ntok, m.chunks);
+    __syncthreads();
   }
 }
 
-__global__ void __launch_bounds__(kBlock) gateup_kernel(GateUpArgs a) {
+template <int BITS>
+__device__ void gateup_tile(const GateUpArgs& a, const uint8_t* blob, const Fmt& f, const int* ent, int nent,
+                            uint8_t* sm) {
+  const int tile = gu_tile_rows(f.H);
+  const int p0 = blockIdx.x * (tile / 2);  // first gate/up row pair of the tile
+  const int npair = min(tile / 2, f.I - p0);
+  if (npair <= 0) return;
+  const int nrows = 2 * npair;
+  // tile row r: pair r / 2, gate row for even r, up row for odd r (the blob's order)
+  stage_rows(sm, [&](int r) { return blob + (size_t)(p0 + (r >> 1)) * f.gu_pair + (size_t)(r & 1) * f.gu_row; },
+             nrows, f.gu_row);
+  float* part = reinterpret_cast<float*>(sm + (size_t)tile * f.gu_row);  // [kTok][rows][chunks]
+  auto entry = [&](int t) { return ent ? ent[t] : t * a.nslots; };       // b * nslots + slot
+  auto vec_of = [&](int t, const uint8_t*& q, const float2*& e) {
+    const int b = entry(t) / a.nslots;
+    q = a.xq + (size_t)b * f.ng_h * kLimbBytes;
+    e = a.xe + (size_t)b * f.ng_h;
+  };
+  auto finish = [&](int t0, int ntok, int chunks) {
+    for (int j = threadIdx.x; j < ntok * npair; j += blockDim.x) {
+      const int t = j / npair, pp = j - t * npair;
+      float g = 0.f, u = 0.f;
+      for (int c = 0; c < chunks; ++c) {
+        g += part[(t * nrows + 2 * pp) * chunks + c];
+        u += part[(t * nrows + 2 * pp + 1) * chunks + c];
+      }
+      a.a_out[(size_t)entry(t0 + t) * f.I + p0 + pp] = silu_mul(g, u);
+    }
+  };
+  tile_tokens<BITS, kMaxRowsPerLane>(sm, f.gu_row, f.gu_codes, f.ng_h, nrows, nent, vec_of, part, finish);
+}
+
+__global__ void __launch_bounds__(kWsThreads, 2) gateup_kernel(GateUpArgs a) {
+  extern __shared__ __align__(16) uint8_t sm[];
   int item = blockIdx.y;
   const uint8_t* blob;
   const int* ent = nullptr;
@@ -338,39 +428,38 @@ __global__ void __launch_bounds__(kBlock) gateup_kernel(GateUpArgs a) {
   }
   const Fmt f = make_fmt(bits, a.H, a.I);
   if (bits == 4)
-    gateup_item<4>(a, blob, f, ent, nent);
+    gateup_tile<4>(a, blob, f, ent, nent, sm);
   else
-    gateup_item<2>(a, blob, f, ent, nent);
+    gateup_tile<2>(a, blob, f, ent, nent, sm);
 }
 
-// ---------------------------------------------------------------------------
-// grouped down: d[b][slot][j] = Wd_j . a[b][slot]
-// ---------------------------------------------------------------------------
 template <int BITS>
-__device__ void down_item(const DownArgs& a, const uint8_t* blob, const Fmt& f, const int* ent, int nent) {
-  __shared__ float part[kRowsD * 4];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int j0 = blockIdx.x * kRowsD;
-  const int nr = min(kRowsD, f.H - j0);
-  if (nr <= 0) return;
-  const RowMap m = make_rowmap(f.ng_i);
-  const uint8_t* rows = blob + f.d_off + (size_t)j0 * f.d_row;
-  auto off = [&](int r) { return (size_t)r * f.d_row; };
-  for (int t = 0; t < nent; ++t) {
-    const int e = ent ? ent[t] : t * a.nslots;
-    rows_dot<BITS>(rows, off, nr, f.ng_i, f.d_codes, a.aq + (size_t)e * f.ng_i * kLimbBytes, a.ae + (size_t)e * f.ng_i,
-                   part, wid, nw, lane);
-    __syncthreads();
-    for (int r = threadIdx.x; r < nr; r += blockDim.x) {
-      float s = 0.f;
-      for (int c = 0; c < m.chunks; ++c) s += part[r * m.chunks + c];
-      a.d_out[(size_t)e * f.H + j0 + r] = s;
+__device__ void down_tile(const DownArgs& a, const uint8_t* blob, const Fmt& f, const int* ent, int nent, uint8_t* sm) {
+  const int tile = dn_tile_rows(f.I);
+  const int j0 = blockIdx.x * tile;
+  const int nrows = min(tile, f.H - j0);
+  if (nrows <= 0) return;
+  stage_rows(sm, [&](int r) { return blob + f.d_off + (size_t)(j0 + r) * f.d_row; }, nrows, f.d_row);
+  float* part = reinterpret_cast<float*>(sm + (size_t)tile * f.d_row);  // [kTok][rows][chunks]
+  auto entry = [&](int t) { return ent ? ent[t] : t * a.nslots; };
+  auto vec_of = [&](int t, const uint8_t*& q, const float2*& e) {
+    const int en = entry(t);
+    q = a.aq + (size_t)en * f.ng_i * kLimbBytes;
+    e = a.ae + (size_t)en * f.ng_i;
+  };
+  auto finish = [&](int t0, int ntok, int chunks) {
+    for (int j = threadIdx.x; j < ntok * nrows; j += blockDim.x) {
+      const int t = j / nrows, r = j - t * nrows;
+      float sum = 0.f;
+      for (int c = 0; c < chunks; ++c) sum += part[(t * nrows + r) * chunks + c];
+      a.d_out[(size_t)entry(t0 + t) * f.H + j0 + r] = sum;
     }
-    __syncthreads();
-  }
+  };
+  tile_tokens<BITS, kMaxRowsPerLane>(sm, f.d_row, f.d_codes, f.ng_i, nrows, nent, vec_of, part, finish);
 }
 
-__global__ void __launch_bounds__(kBlock) down_kernel(DownArgs a) {
+__global__ void __launch_bounds__(kWsThreads, 2) down_kernel(DownArgs a) {
+  extern __shared__ __align__(16) uint8_t sm[];
   int item = blockIdx.y;
   const uint8_t* blob;
   const int* ent = nullptr;
@@ -390,9 +479,9 @@ __global__ void __launch_bounds__(kBlock) down_kernel(DownArgs a) {
   }
   const Fmt f = make_fmt(bits, a.H, a.I);
   if (bits == 4)
-    down_item<4>(a, blob, f, ent, nent);
+    down_tile<4>(a, blob, f, ent, nent, sm);
   else
-    down_item<2>(a, blob, f, ent, nent);
+    down_tile<2>(a, blob, f, ent, nent, sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -437,7 +526,8 @@ cudaError_t launch_norm_quant(const NormQuantArgs& a, int B, cudaStream_t s) {
 }
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   const int rows = a.E + (a.gate ? 1 : 0);
-  router_kernel<<<(rows + 7) / 8, 256, 0, s>>>(a);
+  dim3 grid((rows + kRtRows - 1) / kRtRows, (a.B + kRtTok - 1) / kRtTok);
+  router_kernel<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 cudaError_t launch_topk(const TopkArgs& a, int B, cudaStream_t s) {
@@ -448,14 +538,37 @@ cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t s) {
   bucket_kernel<<<1, kBlock, (size_t)(2 * a.E + 1) * sizeof(int), s>>>(a);
   return cudaGetLastError();
 }
+// shared memory of one weight-stationary tile: staged rows and the partials of
+// one token chunk ([kTok][rows][row chunks]); sized for the wider code width
+static size_t tile_smem(int rows, int row_bytes_4, int row_bytes_2, int ng) {
+  return (size_t)rows * std::max(row_bytes_4, row_bytes_2) + (size_t)kTok * rows * ((ng + 31) / 32) * 4;
+}
 cudaError_t launch_gateup(const GateUpArgs& a, int items, cudaStream_t s) {
-  dim3 grid((a.I + kRowsGU - 1) / kRowsGU, items);
-  gateup_kernel<<<grid, kBlock, 0, s>>>(a);
+  const int tile = gu_tile_rows(a.H);
+  if (tile < 2) return cudaErrorInvalidValue;
+  const size_t sm = tile_smem(tile, make_fmt(4, a.H, a.I).gu_row, make_fmt(2, a.H, a.I).gu_row, a.H / kGroup);
+  static int configured = -1;
+  if (sm > 48 * 1024 && (int)sm > configured) {
+    cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    configured = (int)sm;
+  }
+  dim3 grid((a.I + tile / 2 - 1) / (tile / 2), items);
+  gateup_kernel<<<grid, kWsThreads, sm, s>>>(a);
   return cudaGetLastError();
 }
 cudaError_t launch_down(const DownArgs& a, int items, cudaStream_t s) {
-  dim3 grid((a.H + kRowsD - 1) / kRowsD, items);
-  down_kernel<<<grid, kBlock, 0, s>>>(a);
+  const int tile = dn_tile_rows(a.I);
+  if (tile < 1) return cudaErrorInvalidValue;
+  const size_t sm = tile_smem(tile, make_fmt(4, a.H, a.I).d_row, make_fmt(2, a.H, a.I).d_row, a.I / kGroup);
+  static int configured = -1;
+  if (sm > 48 * 1024 && (int)sm > configured) {
+    cudaError_t e = cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    configured = (int)sm;
+  }
+  dim3 grid((a.H + tile - 1) / tile, items);
+  down_kernel<<<grid, kWsThreads, sm, s>>>(a);
   return cudaGetLastError();
 }
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
