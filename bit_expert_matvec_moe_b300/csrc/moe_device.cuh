@@ -223,21 +223,30 @@ __device__ __forceinline__ void zero_limbs(Limbs& L) {
 // out above; c1 unused for 2-bit), returned as an fp32 value before 2^(e-22).
 template <int BITS>
 __device__ __forceinline__ float group_dot(const uint4 c0, const uint4 c1, const Limbs& L) {
-  uint32_t a0 = 0u, a1 = 0u;
-  int a2 = 0;
   if (BITS == 4) {
+    // low nibbles as bytes, high nibbles in place (bytes 16 * code): the b*
+    // sums are exactly 16 times the high-nibble sums, so no shift per word
+    uint32_t a0 = 0u, a1 = 0u, b0 = 0u, b1 = 0u;
+    int a2 = 0, b2 = 0;
     const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const uint32_t lo = w[q] & 0x0F0F0F0Fu, hi = (w[q] >> 4) & 0x0F0F0F0Fu;
+      const uint32_t lo = w[q] & 0x0F0F0F0Fu, hi = w[q] & 0xF0F0F0F0u;
       a0 = dp4a_uu(lo, L.w[6 * q + 0], a0);
-      a0 = dp4a_uu(hi, L.w[6 * q + 1], a0);
+      b0 = dp4a_uu(hi, L.w[6 * q + 1], b0);
       a1 = dp4a_uu(lo, L.w[6 * q + 2], a1);
-      a1 = dp4a_uu(hi, L.w[6 * q + 3], a1);
+      b1 = dp4a_uu(hi, L.w[6 * q + 3], b1);
       a2 = dp4a_us(lo, L.w[6 * q + 4], a2);
-      a2 = dp4a_us(hi, L.w[6 * q + 5], a2);
+      b2 = dp4a_us(hi, L.w[6 * q + 5], b2);
     }
+    // limbs 0 and 1 combine exactly in int32 (< 2^26); the b parts are
+    // multiples of 16, so the shifts are exact
+    const int t01 = (int)(a0 + (a1 << 8)) + (int)((b0 + (b1 << 8)) >> 4);
+    const int t2 = a2 + (b2 >> 4);
+    return fmaf((float)t2, 65536.f, (float)t01);
   } else {
+    uint32_t a0 = 0u, a1 = 0u;
+    int a2 = 0;
     const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -252,9 +261,8 @@ __device__ __forceinline__ float group_dot(const uint4 c0, const uint4 c1, const
         a2 = dp4a_us(f[t], L.w[base + 4], a2);
       }
     }
+    return fmaf((float)a2, 65536.f, (float)(int)(a0 + (a1 << 8)));
   }
-  // a2 * 65536 and a1 * 256 + a0 are exact in fp32; their sum rounds once
-  return fmaf((float)a2, 65536.f, fmaf((float)a1, 256.f, (float)a0));
 }
 
 // Partial row dot of one lane: group g of a quantised row (codes at `row`,

@@ -119,21 +119,22 @@ __global__ void __launch_bounds__(kBlock) norm_quant_kernel(NormQuantArgs a) {
 // ---------------------------------------------------------------------------
 // Tiled over (router rows, tokens): a block computes kRtRows rows x kRtTok
 // tokens, staging chunks of kRtK inputs of the rows (bf16) and of the tokens'
-// xn (fp32) in shared memory (rows padded by one word, so that the threads of
-// a warp, which read different rows or tokens at the same input, hit different
-// banks).  Thread t owns row t / 8 and tokens t % 8, t % 8 + 8; each output is
-// a fixed-order sum (four interleaved partial sums per chunk, added pairwise,
-// then chunk by chunk), so results do not depend on scheduling and rounding
-// chains stay short.
-constexpr int kRtRows = 32, kRtTok = 16, kRtK = 256;
+// xn (fp32) in shared memory (rows padded by one word against bank
+// conflicts).  Four adjacent threads share one output, each taking every
+// fourth input pair with two interleaved partial sums; the four are combined by
+// shuffles in a fixed order, so results do not depend on scheduling and
+// rounding chains stay short.
+constexpr int kRtRows = 8, kRtTok = 8, kRtK = 256, kRtSplit = 4;
+static_assert(kRtRows * kRtTok * kRtSplit == 256, "router block shape");
 __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
   __shared__ float xs[kRtTok][kRtK + 1];
   __shared__ uint32_t rs[kRtRows][kRtK / 2 + 1];  // bf16 pairs
   const int tid = threadIdx.x;
   const int nrows = a.E + (a.gate ? 1 : 0);
   const int row0 = blockIdx.x * kRtRows, b0 = blockIdx.y * kRtTok;
-  const int lr = tid >> 3, lt = tid & 7;
-  float acc0 = 0.f, acc1 = 0.f;
+  const int o = tid / kRtSplit, q = tid % kRtSplit;  // output o: row o / kRtTok, token o % kRtTok
+  const int lr = o / kRtTok, lt = o % kRtTok;
+  float acc = 0.f;
   for (int k0 = 0; k0 < a.H; k0 += kRtK) {
     const int kn = min(kRtK, a.H - k0);  // a multiple of 64
     for (int i = tid; i < kRtTok * (kn / 4); i += 256) {
@@ -153,32 +154,22 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
       rs[r][c / 2] = v.x; rs[r][c / 2 + 1] = v.y; rs[r][c / 2 + 2] = v.z; rs[r][c / 2 + 3] = v.w;
     }
     __syncthreads();
-    // four interleaved partial sums per chunk, added pairwise: short rounding chains
-    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c = 0; c < kn / 2; c += 4) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t w = rs[lr][c + q];
-        const float r0 = bf16lo(w), r1 = bf16hi(w);
-        p0[q] = fmaf(r1, xs[lt][2 * (c + q) + 1], fmaf(r0, xs[lt][2 * (c + q)], p0[q]));
-        p1[q] = fmaf(r1, xs[lt + 8][2 * (c + q) + 1], fmaf(r0, xs[lt + 8][2 * (c + q)], p1[q]));
-      }
+    float p0 = 0.f, p1 = 0.f;
+    for (int c = q; c < kn / 2; c += 2 * kRtSplit) {  // pairs c and c + kRtSplit (kn / 2 is a multiple of 8)
+      const uint32_t w0 = rs[lr][c], w1 = rs[lr][c + kRtSplit];
+      p0 = fmaf(bf16hi(w0), xs[lt][2 * c + 1], fmaf(bf16lo(w0), xs[lt][2 * c], p0));
+      p1 = fmaf(bf16hi(w1), xs[lt][2 * (c + kRtSplit) + 1], fmaf(bf16lo(w1), xs[lt][2 * (c + kRtSplit)], p1));
     }
-    acc0 += (p0[0] + p0[1]) + (p0[2] + p0[3]);
-    acc1 += (p1[0] + p1[1]) + (p1[2] + p1[3]);
+    acc += p0 + p1;
     __syncthreads();
   }
-  const int row = row0 + lr;
-  if (row < nrows) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int b = b0 + lt + 8 * j;
-      if (b < a.B) {
-        float v = j == 0 ? acc0 : acc1;
-        if (row < a.E && a.offset) v += a.offset[(size_t)b * a.E + row];
-        a.logits[(size_t)b * (a.E + 1) + row] = v;
-      }
-    }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  const int row = row0 + lr, b = b0 + lt;
+  if (q == 0 && row < nrows && b < a.B) {
+    float v = acc;
+    if (row < a.E && a.offset) v += a.offset[(size_t)b * a.E + row];
+    a.logits[(size_t)b * (a.E + 1) + row] = v;
   }
 }
 
