@@ -4,35 +4,37 @@
 // [c*H/P, (c+1)*H/P) of every expert the token uses, and router rows
 // [c*E/P, (c+1)*E/P).  Its weight bytes arrive by bulk copies (TMA engine)
 // into shared memory, each with its own mbarrier:
-//   start         router rows, shared expert gate/up rows and down rows
-//   after top-K   gate/up rows of all K routed experts, then their down rows,
-//                 all issued at once (they fit beside each other)
-// Grid-wide data dependencies use split-phase barriers in the workspace header
-// (arrive when a block has published, wait only where the data is consumed):
-//   L     every block wrote its router logits          -> top-K
-//   S     every block wrote its slice of a_shared      -> shared down rows
-//   R_k   every block wrote its slice of a_k           -> routed down rows
+//   start           h, router rows, shared expert gate/up rows and down rows
+//   after top-K     gate/up rows of all K routed experts (they fit side by side)
+//   after gate/up k down rows of routed expert k (once its gate/up rows landed)
+// Grid-wide data dependencies go through the workspace: every published word
+// carries the launch's epoch in its upper half (a reader sees either the old
+// word or the new one, never a mix), and one relaxed counter per exchange
+// (logits; activations) tells a reader when every block has published.
 // Phases of a block:
-//   h -> limbs of h*gamma (the RMS factor r is applied to each dot product,
-//        so quantisation does not wait for the norm); r from a block sum
-//   router rows -> logits, arrive L
-//   shared gate/up + SwiGLU -> a_shared slice, arrive S
-//   wait L; top-K by one warp (every block, same result); issue routed copies
-//   routed gate/up + SwiGLU -> a_k slices, arrive R_k (as each expert lands)
-//   wait S and every R_k; limbs of every a; down rows of every expert -> y
-//   h[rows] += y
+//   h -> limbs of h*gamma (the RMS factor r multiplies each gate/up dot
+//        product, so quantisation does not wait for the norm); r from a block sum
+//   router rows -> published logits
+//   shared expert gate/up (all warps)
+//   warp 0: wait for every block's logits; top-K (every block, same result);
+//           issue the routed gate/up copies; softmax over the chosen
+//   routed gate/up rows expert by expert as their copies land
+//   SwiGLU of every expert's rows, times its routing weight -> published
+//   wait for every block's activations; one bulk copy; limbs of each 64-group
+//   down rows of every expert as one long dot product per row -> h[rows] += y
 // Routing never leaves the device.  Every wait is bounded (1 s): on timeout the
-// block records MOE_ERR_TIMEOUT, waits (bounded) for its own copies in flight
-// and leaves; later launches on the same workspace return at once until the
-// status word is read.  Nothing lives in local memory: with ~227 KB of shared
-// memory per block the L1 cache is small, and spilled state would go to L2.
+// block records MOE_ERR_TIMEOUT, waits (bounded) for its own copies in flight,
+// advances the counters it still owes and leaves; later launches on the same
+// workspace return at once until the status word is read.  Nothing lives in
+// local memory: with ~227 KB of shared memory per block the L1 cache is small,
+// and spilled state would go to L2.
 //
 // Limits of this kernel (the host falls back to the multi-kernel path outside
 // them): hidden <= 4096, inter <= 2048, experts <= 1024, top-K <= 8, and the
 // plan must fit in shared memory.
 //
-// With programmatic dependent launch (kPDL) the weight copies of the prologue
-// are issued before griddepcontrol.wait, i.e. while the previous kernel on the
+// With programmatic dependent launch (kPDL) the shared expert's rows are
+// copied before griddepcontrol.wait, i.e. while the previous kernel on the
 // stream may still run; nothing the caller writes (h, offsets, workspace) is
 // read before that wait.
 #include "moe_internal.h"
