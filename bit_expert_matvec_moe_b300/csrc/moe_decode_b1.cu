@@ -726,14 +726,11 @@ bool decode_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s) {
-  static int configured_bytes[2] = {-1, -1};
+  static std::atomic<int> configured[2][kMaxDevices];  // per PDL variant and device
   const int bytes = (int)a.plan.total;
-  if (bytes > 48 * 1024 && bytes > configured_bytes[pdl]) {
-    cudaError_t e = pdl ? cudaFuncSetAttribute(decode_b1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
-                        : cudaFuncSetAttribute(decode_b1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    configured_bytes[pdl] = bytes;
-  }
+  const cudaError_t e = pdl ? ensure_dynamic_smem(decode_b1_kernel<true>, bytes, configured[1])
+                            : ensure_dynamic_smem(decode_b1_kernel<false>, bytes, configured[0]);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.plan.P);
   cfg.blockDim = dim3(kBlock);

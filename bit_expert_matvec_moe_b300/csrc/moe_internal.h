@@ -2,6 +2,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <cstddef>
 #include <string>
 #include <cstdint>
@@ -162,5 +163,22 @@ cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s);
 
 // Text returned by moe_last_error_message() for this thread.
 void set_last_error(const std::string& msg);
+
+// Opt-in dynamic shared memory of a kernel, raised once per device to the
+// largest size launched so far (the attribute is per device; calls from
+// several threads at once only repeat the same setting).
+constexpr int kMaxDevices = 64;
+template <typename Kernel>
+cudaError_t ensure_dynamic_smem(Kernel kernel, int bytes, std::atomic<int> (&configured)[kMaxDevices]) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (configured[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) configured[dev].store(bytes, std::memory_order_relaxed);
+  return e;
+}
 
 }  // namespace moe

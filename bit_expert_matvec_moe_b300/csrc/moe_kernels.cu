@@ -538,12 +538,9 @@ cudaError_t launch_gateup(const GateUpArgs& a, int items, cudaStream_t s) {
   const int tile = gu_tile_rows(a.H);
   if (tile < 2) return cudaErrorInvalidValue;
   const size_t sm = tile_smem(tile, make_fmt(4, a.H, a.I).gu_row, make_fmt(2, a.H, a.I).gu_row, a.H / kGroup);
-  static int configured = -1;
-  if (sm > 48 * 1024 && (int)sm > configured) {
-    cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    configured = (int)sm;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  const cudaError_t e = ensure_dynamic_smem(gateup_kernel, (int)sm, configured);
+  if (e != cudaSuccess) return e;
   dim3 grid((a.I + tile / 2 - 1) / (tile / 2), items);
   gateup_kernel<<<grid, kWsThreads, sm, s>>>(a);
   return cudaGetLastError();
@@ -552,12 +549,9 @@ cudaError_t launch_down(const DownArgs& a, int items, cudaStream_t s) {
   const int tile = dn_tile_rows(a.I);
   if (tile < 1) return cudaErrorInvalidValue;
   const size_t sm = tile_smem(tile, make_fmt(4, a.H, a.I).d_row, make_fmt(2, a.H, a.I).d_row, a.I / kGroup);
-  static int configured = -1;
-  if (sm > 48 * 1024 && (int)sm > configured) {
-    cudaError_t e = cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    configured = (int)sm;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  const cudaError_t e = ensure_dynamic_smem(down_kernel, (int)sm, configured);
+  if (e != cudaSuccess) return e;
   dim3 grid((a.H + tile - 1) / tile, items);
   down_kernel<<<grid, kWsThreads, sm, s>>>(a);
   return cudaGetLastError();

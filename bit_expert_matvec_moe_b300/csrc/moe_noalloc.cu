@@ -21,7 +21,6 @@ using namespace moe;
 namespace {
 
 constexpr size_t kScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // header, then published logits, then published activations (the single-token
 // kernel's cross-block state); zeroed once per device at set-up
