@@ -63,6 +63,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value: the job's time is its slowest rank's."""
+    if world <= 1:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -251,11 +267,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     ck = clocks.stop()
     assert M.moe_get_device_status(ws, stream) == 0
-    ms = float(np.mean(step_ms))
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.mean(step_ms)), world, "cuda")
 
     # end to end through the public API with host buffers: H2D of the step's
     # hidden states from pinned memory, the decode calls, D2H of the outputs
@@ -275,7 +287,7 @@ def run_ours(args, rank, world, local):
             e1.synchronize()
             if it >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
-    e2e = float(np.mean(e2e_ms))
+    e2e = max_over_ranks(float(np.mean(e2e_ms)), world, "cuda")
 
     # unique routed experts per call (each streamed once for all of the call's tokens)
     idx_h = idx[: nsteps_tok * B].cpu().numpy().reshape(nsteps_tok, B * d.top_k)
@@ -286,7 +298,7 @@ def run_ours(args, rank, world, local):
     router_bytes = d.n_experts * d.hidden * 2
     launches_per_step = nsteps_tok
     per_launch_s = ms / 1e3 / launches_per_step
-    tok_s = T * world / (ms / 1e3)
+    tok_s = job_throughput(T, world, ms)
     peak, peak_kind = measured_hbm_peak()
     alg = int(call_bytes + router_bytes)
     achieved = (call_bytes + router_bytes) / per_launch_s / 1e9
@@ -326,7 +338,7 @@ def run_ours(args, rank, world, local):
             "algorithmic_bytes_per_launch": alg,
             "traffic": profiled_traffic("decode_b1_full_b1") if (B == 1 and bits == 4) else None,
         },
-        "e2e": {"value": round(T * world / (e2e / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(T, world, e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_pin.numel() * 4), "d2h_bytes_per_step": int(y_pin.numel() * 4 + idx_pin.numel() * 4)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": ck,
@@ -404,6 +416,8 @@ def run_stack(args, rank, world, local):
             h.copy_(h0)
             graph.replay()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -420,7 +434,7 @@ def run_stack(args, rank, world, local):
     torch.cuda.synchronize()
     ck = clocks.stop()
     assert M.moe_get_device_status(ws, stream) == 0
-    ms = float(np.mean(step_ms))
+    ms = max_over_ranks(float(np.mean(step_ms)), world, "cuda")
     # end to end: H2D of the step's hidden states, the 40-layer pass of every token, D2H of the outputs
     h_pin = torch.from_numpy(h_host).pin_memory()
     y_pin = torch.empty_like(h_pin).pin_memory()
@@ -436,9 +450,9 @@ def run_stack(args, rank, world, local):
             e1.synchronize()
             if it >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
-    e2e = float(np.mean(e2e_ms))
+    e2e = max_over_ranks(float(np.mean(e2e_ms)), world, "cuda")
     layer_bytes = (K + 1) * M.moe_packed_expert_bytes(d, 4) + E * d.hidden * 2
-    tok_s = T * world / (ms / 1e3)
+    tok_s = job_throughput(T, world, ms)
     per_launch_s = ms / 1e3 / (T * Lyr)
     peak, peak_kind = measured_hbm_peak()
     achieved = layer_bytes / per_launch_s / 1e9
@@ -470,7 +484,7 @@ def run_stack(args, rank, world, local):
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "algorithmic_bytes_per_launch": int(layer_bytes), "traffic": None,
         },
-        "e2e": {"value": round(T * world / (e2e / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(T, world, e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_pin.numel() * 4), "d2h_bytes_per_step": int(y_pin.numel() * 4)},
         "gpu_launches": T * Lyr * args.steps,
         "clocks": ck,
