@@ -63,8 +63,9 @@ WsLayout ws_layout(const moe_dims& d, int B) {
   L.ae = take(B * ns * ngi * 8);
   L.d = take(B * ns * H * 4);
   L.nuniq = take(4);
-  L.uniq_e = take((E + 1) * 4);
-  L.uniq_off = take((E + 2) * 4);
+  const size_t shared_items = (B + kSharedChunk - 1) / kSharedChunk;  // the shared expert's work items
+  L.uniq_e = take((E + shared_items) * 4);
+  L.uniq_off = take((E + shared_items + 1) * 4);
   L.ent = take(B * ns * 4);
   // published words of the single-token kernel (epoch << 32 | value)
   L.pub_logits = take((E + 1) * 8);
@@ -346,7 +347,7 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   bk.uniq_off = at<int>(ws, L.uniq_off);
   bk.ent = at<int>(ws, L.ent);
   if ((e = launch_bucket(bk, s)) != cudaSuccess) return cuda_fail(e);
-  const int items = std::min(B * K, E) + has_shared;
+  const int items = std::min(B * K, E) + (has_shared ? (B + kSharedChunk - 1) / kSharedChunk : 0);
 
   GateUpArgs g{};
   g.H = H;

@@ -14,6 +14,7 @@ namespace moe {
 
 constexpr int kBlock = 512;   // threads per block of the matvec kernels
 constexpr int kWarps = kBlock / 32;
+constexpr int kSharedChunk = 32;  // batched path: shared-expert tokens per work item
 
 
 struct PackArgs {

@@ -211,21 +211,35 @@ __global__ void __launch_bounds__(32) topk_kernel(TopkArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// token -> expert grouping (one block): every touched expert is listed once,
-// ascending by id, with its (token, slot) entries ascending by token; the shared
-// expert, when present, is the last item and holds every token at slot K.
+// token -> expert grouping (one block).  Work items: first the shared expert,
+// when present, in items of at most kSharedChunk tokens (slot K of every token:
+// the heaviest items, so they are dispatched first and spread over more
+// blocks), then every touched routed expert once, ascending by id, with its
+// (token, slot) entries ascending by token.  Item u covers entries
+// [uniq_off[u], uniq_off[u + 1]); expert id -1 is the shared expert.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kBlock) bucket_kernel(BucketArgs a) {
   extern __shared__ int bk_smem[];
-  int* cnt = bk_smem;            // [E]
-  int* off = cnt + a.E;          // [E + 1]
   const int n = a.B * a.K;
+  int* cnt = bk_smem;     // [E]
+  int* off = cnt + a.E;   // [E]
+  int* ids = off + a.E;   // [n] the routing choices, staged
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) cnt[e] = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) ids[i] = a.idx[i];
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&cnt[a.idx[i]], 1);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&cnt[ids[i]], 1);
   __syncthreads();
   if (threadIdx.x == 0) {
-    int run = 0, u = 0;
+    int u = 0, base = 0;
+    if (a.has_shared) {
+      for (int b0 = 0; b0 < a.B; b0 += kSharedChunk) {
+        a.uniq_e[u] = -1;
+        a.uniq_off[u] = b0;
+        ++u;
+      }
+      base = a.B;
+    }
+    int run = base;
     for (int e = 0; e < a.E; ++e) {
       off[e] = run;
       if (cnt[e] > 0) {
@@ -235,29 +249,21 @@ __global__ void __launch_bounds__(kBlock) bucket_kernel(BucketArgs a) {
       }
       run += cnt[e];
     }
-    off[a.E] = run;
-    int nu = u;
-    if (a.has_shared) {
-      a.uniq_e[u] = -1;  // shared expert
-      a.uniq_off[u] = run;
-      nu = u + 1;
-      run += a.B;
-    }
-    a.uniq_off[nu] = run;
-    *a.n_uniq = nu;
+    a.uniq_off[u] = run;
+    *a.n_uniq = u;
   }
   __syncthreads();
   // entry i = (b, k): its position among entries of the same expert is the
   // number of earlier entries (in (b, k) order) with that expert
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int e = a.idx[i];
+    const int e = ids[i];
     int pos = 0;
-    for (int j = 0; j < i; ++j) pos += (a.idx[j] == e);
+    for (int j = 0; j < i; ++j) pos += (ids[j] == e);
     const int b = i / a.K, k = i % a.K;
     a.ent[off[e] + pos] = b * a.nslots + k;
   }
   if (a.has_shared)
-    for (int b = threadIdx.x; b < a.B; b += blockDim.x) a.ent[off[a.E] + b] = b * a.nslots + a.K;
+    for (int b = threadIdx.x; b < a.B; b += blockDim.x) a.ent[b] = b * a.nslots + a.K;
 }
 
 // ---------------------------------------------------------------------------
@@ -526,7 +532,9 @@ cudaError_t launch_topk(const TopkArgs& a, int B, cudaStream_t s) {
   return cudaGetLastError();
 }
 cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t s) {
-  bucket_kernel<<<1, kBlock, (size_t)(2 * a.E + 1) * sizeof(int), s>>>(a);
+  const size_t sm = (size_t)(2 * a.E + a.B * a.K) * sizeof(int);
+  if (sm > 48 * 1024) return cudaErrorInvalidValue;
+  bucket_kernel<<<1, kBlock, sm, s>>>(a);
   return cudaGetLastError();
 }
 // shared memory of one weight-stationary tile: staged rows and the partials of
