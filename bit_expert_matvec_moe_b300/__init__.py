@@ -48,16 +48,55 @@ class Dims:
                           self.rms_eps, self.flags)
 
 
-def _ptr(t) -> int | None:
+# element types the C ABI expects, by argument kind (dtype names of torch)
+_KINDS = {
+    "f32": ("float32",),
+    "i32": ("int32",),
+    "b16": ("int16", "uint16", "bfloat16"),  # bf16 bit patterns
+    "u8": ("uint8", "int8"),
+}
+
+
+def _check_type(t, name: str, kind: str | None = None, numel: int | None = None) -> None:
+    """Element type (kind) and size (at least `numel` elements) of a tensor argument."""
+    if t is None or isinstance(t, int):
+        return
+    if kind is not None:
+        dt = str(t.dtype).replace("torch.", "")
+        if dt not in _KINDS[kind]:
+            raise ValueError(f"{name}: expected dtype {' or '.join(_KINDS[kind])}, got {dt}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name}: expected at least {numel} elements, got {t.numel()}")
+
+
+def _ptr(t, name: str = "tensor", kind: str | None = None, numel: int | None = None) -> int | None:
+    """Device pointer of a contiguous CUDA tensor (an integer is taken as a
+    pointer as it is), after the checks of _check_type."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    _check_type(t, name, kind, numel)
     if not t.is_cuda:
-        raise ValueError("expected a CUDA tensor")
+        raise ValueError(f"{name}: expected a CUDA tensor")
     if not t.is_contiguous():
-        raise ValueError("expected a contiguous tensor")
+        raise ValueError(f"{name}: expected a contiguous tensor")
     return t.data_ptr()
+
+
+def _ptrs(*specs) -> list:
+    """Pointers of several arguments (tensor, name, kind, numel): every type
+    and size is checked first, so the error names the argument that is wrong."""
+    for spec in specs:
+        _check_type(*spec)
+    return [_ptr(*spec) for spec in specs]
+
+
+def _rows(t, name: str, cols: int) -> int:
+    """Rows of a [B, cols] tensor."""
+    if t.dim() != 2 or t.shape[1] != cols:
+        raise ValueError(f"{name}: expected shape [B, {cols}], got {list(t.shape)}")
+    return int(t.shape[0])
 
 
 def _stream(stream=None) -> int:
@@ -87,24 +126,29 @@ def moe_workspace_init(ws, stream=None) -> None:
 def moe_pack_weights(dims: Dims, bits: int, codes, scales, biases, dst, stream=None) -> None:
     """codes/scales/biases: three tensors each (gate, up, down), canonical layout."""
     VP3 = ctypes.c_void_p * 3
-    c = VP3(*[_ptr(t) for t in codes])
-    s = VP3(*[_ptr(t) for t in scales])
-    b = VP3(*[_ptr(t) for t in biases])
+    ptrs = _ptrs(*[(t, "codes", "u8", None) for t in codes], *[(t, "scales", "b16", None) for t in scales],
+                 *[(t, "biases", "b16", None) for t in biases])
+    c, s, b = VP3(*ptrs[0:3]), VP3(*ptrs[3:6]), VP3(*ptrs[6:9])
     _check(N.load().moe_pack_weights(ctypes.byref(dims.c()), bits, c, s, b, _ptr(dst), _stream(stream)),
            "moe_pack_weights")
 
 
 def moe_route(dims: Dims, xn, router, idx, w, ws, logit_offset=None, logits_out=None, stream=None) -> None:
-    B = xn.shape[0]
-    _check(N.load().moe_route(ctypes.byref(dims.c()), _ptr(xn), B, _ptr(router), _ptr(logit_offset), _ptr(idx),
-                              _ptr(w), _ptr(logits_out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+    B = _rows(xn, "xn", dims.hidden)
+    E, K = dims.n_experts, dims.top_k
+    px, pr, po, pi, pw, pl = _ptrs((xn, "xn", "f32", None), (router, "router", "b16", E * dims.hidden),
+                                   (logit_offset, "logit_offset", "f32", B * E), (idx, "idx", "i32", B * K),
+                                   (w, "w", "f32", B * K), (logits_out, "logits_out", "f32", B * E))
+    _check(N.load().moe_route(ctypes.byref(dims.c()), px, B, pr, po, pi, pw, pl, _ptr(ws),
+                              ws.numel() * ws.element_size(), _stream(stream)),
            "moe_route")
 
 
 def moe_expert_forward(dims: Dims, bits: int, blob, xn, out, ws, row_w=None, accumulate: bool = False,
                        stream=None) -> None:
-    B = xn.shape[0]
-    _check(N.load().moe_expert_forward(ctypes.byref(dims.c()), bits, _ptr(blob), _ptr(xn), B, _ptr(row_w), _ptr(out),
+    B = _rows(xn, "xn", dims.hidden)
+    px, prw, po = _ptrs((xn, "xn", "f32", None), (row_w, "row_w", "f32", B), (out, "out", "f32", B * dims.hidden))
+    _check(N.load().moe_expert_forward(ctypes.byref(dims.c()), bits, _ptr(blob), px, B, prw, po,
                                        1 if accumulate else 0, _ptr(ws), ws.numel() * ws.element_size(),
                                        _stream(stream)),
            "moe_expert_forward")
@@ -113,14 +157,23 @@ def moe_expert_forward(dims: Dims, bits: int, blob, xn, out, ws, row_w=None, acc
 def make_layer(dims: Dims, experts, expert_stride: int, router, shared=None, shared_bits: int = 4, rms_gamma=None,
                shared_gate=None) -> N.moe_layer:
     """A C moe_layer that refers to the given device tensors (keep them alive)."""
-    return N.moe_layer(dims.c(), _ptr(experts), expert_stride, _ptr(shared), shared_bits, _ptr(router),
-                       _ptr(rms_gamma), _ptr(shared_gate))
+    H = dims.hidden
+    pr, pg, ps = _ptrs((router, "router", "b16", dims.n_experts * H), (rms_gamma, "rms_gamma", "b16", H),
+                       (shared_gate, "shared_gate", "b16", H))
+    return N.moe_layer(dims.c(), _ptr(experts), expert_stride, _ptr(shared), shared_bits, pr, pg, ps)
+
+
+def _layer_io(layer, h, logit_offset, idx_out, w_out):
+    d = layer.d
+    B = _rows(h, "h", d.hidden)
+    return B, _ptrs((h, "h", "f32", None), (logit_offset, "logit_offset", "f32", B * d.n_experts),
+                    (idx_out, "idx_out", "i32", B * d.top_k), (w_out, "w_out", "f32", B * d.top_k))
 
 
 def moe_layer_decode(layer: N.moe_layer, h, ws, logit_offset=None, idx_out=None, w_out=None, stream=None) -> None:
-    B = h.shape[0]
-    _check(N.load().moe_layer_decode(ctypes.byref(layer), _ptr(h), B, _ptr(logit_offset), _ptr(idx_out), _ptr(w_out),
-                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+    B, (ph, po, pi, pw) = _layer_io(layer, h, logit_offset, idx_out, w_out)
+    _check(N.load().moe_layer_decode(ctypes.byref(layer), ph, B, po, pi, pw, _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)),
            "moe_layer_decode")
 
 
@@ -128,10 +181,11 @@ def moe_layer_decode_noalloc(layer: N.moe_layer, h, logit_offset=None, idx_out=N
                              stream=None) -> None:
     """Single-token layer without a caller workspace (the library's fixed
     device array instead; see include/moe.h).  h is [1, hidden]."""
-    if h.shape[0] != 1:
+    B, (ph, po, pi, pw) = _layer_io(layer, h, logit_offset, idx_out, w_out)
+    if B != 1:
         raise ValueError("moe_layer_decode_noalloc takes one token")
-    _check(N.load().moe_layer_decode_noalloc(ctypes.byref(layer), _ptr(h), _ptr(logit_offset), _ptr(idx_out),
-                                             _ptr(w_out), _ptr(status_out), _stream(stream)),
+    _check(N.load().moe_layer_decode_noalloc(ctypes.byref(layer), ph, po, pi, pw, _ptr(status_out, "status_out", "i32", 1),
+                                             _stream(stream)),
            "moe_layer_decode_noalloc")
 
 

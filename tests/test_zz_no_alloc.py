@@ -71,7 +71,8 @@ def test_noalloc_rejects_layers_beyond_its_array():
     d = M.Dims(hidden=4096, inter=4096, n_experts=1024, top_k=8, flags=M.MOE_HAS_SHARED)
     stride = M.moe_packed_expert_bytes(d, 4)
     fake = torch.empty(16, dtype=torch.uint8, device="cuda")
-    layer = M.make_layer(d, fake, stride, fake, shared=fake)
+    router = torch.empty((1024, 4096), dtype=torch.int16, device="cuda")
+    layer = M.make_layer(d, fake, stride, router, shared=fake)
     h = torch.zeros((1, 4096), dtype=torch.float32, device="cuda")
     with pytest.raises(M.MoeError) as err:
         M.moe_layer_decode_noalloc(layer, h)
