@@ -139,7 +139,7 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
  *              least significant bit (low nibble = even element);
  *   scales[m]  bf16 [rows, cols/64];  biases[m] bf16 [rows, cols/64];
  *   weight     W[r][c] = code * scale[r][c/64] + bias[r][c/64]
- *              ("nibble * scale + bias", "Techniques de rupture" item 2).
+ *              (the pages' affine dequantisation, "Techniques de rupture" item 2).
  * dst receives moe_packed_expert_bytes(dims, bits) bytes.  Device pointers;
  * code rows must start 16-byte aligned (cols*bits/8 a multiple of 16).
  */
@@ -157,8 +157,8 @@ moe_status moe_pack_weights(const moe_dims* dims, int32_t bits,
  *                 over the K chosen (so the weights of a token sum to 1).
  * xn fp32 [B, hidden] is the normalised hidden state; logit_offset fp32
  * [B, n_experts] or NULL; idx int32 [B, K]; w fp32 [B, K]; logits_out fp32
- * [B, n_experts] or NULL.  The pages route on the CPU ("Pipeline GPU
- * différé": "CPU : routage"); here routing stays on the device.
+ * [B, n_experts] or NULL.  The pages route on the CPU ("Techniques de
+ * rupture" item 3, the deferred GPU pipeline); here routing stays on the device.
  */
 moe_status moe_route(const moe_dims* dims, const float* xn, int32_t B,
                      const uint16_t* router, const float* logit_offset,
@@ -184,8 +184,12 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
  * with g_s = 1, or sigmoid(shared_gate . xn) under MOE_HAS_SHARED_GATE.
  * logit_offset fp32 [B, n_experts] or NULL is added to the router logits.
  * idx_out int32 [B, K] and w_out fp32 [B, K] receive the routing, or NULL.
- * B == 1 runs one cooperative persistent kernel; B > 1 groups the tokens by
- * expert so that each touched expert is streamed once per call.
+ * B == 1 runs one persistent kernel, one block per SM (a cooperative launch,
+ * or under MOE_PDL a programmatic dependent launch) when the shape fits it
+ * (hidden <= 4096, inter <= 2048, experts <= 1024, top_k <= 8), else the
+ * multi-kernel path; B > 1 groups the tokens by expert so that each touched
+ * expert is streamed once per call (the shared expert first, in pieces of at
+ * most 32 tokens).
  */
 moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B,
                             const float* logit_offset, int32_t* idx_out, float* w_out,
