@@ -10,8 +10,8 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_decode_b1.cu", "moe_noalloc.cu"]
-HEADERS = ["moe_device.cuh", "moe_internal.h"]
+SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_decode_b1.cu", "moe_noalloc.cu", "moe_tc.cu"]
+HEADERS = ["moe_device.cuh", "moe_internal.h", "moe_tc.cuh"]
 LIB = os.path.join(HERE, "libmoe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-ftz=false", "-prec-div=true",

@@ -5,7 +5,9 @@ tests and the bench use and 3000 random shapes inside its limits (regions
 aligned, disjoint and inside the total, per-block rows and copies inside their
 slots, every row covered by the lane and thread mappings); tests/tile_check.cu
 checks the batched path's tiles for every hidden and inter size the ABI
-accepts."""
+accepts; tests/tc_check.cu checks the tensor-core contraction's unpacking
+tables against the packed format, its descriptor encodings, swizzle and
+shared-memory plan."""
 import os
 import shutil
 import subprocess
@@ -44,3 +46,7 @@ def test_single_token_plan_invariants(tmp_path):
 
 def test_batched_tile_geometry(tmp_path):
     _build_and_run(tmp_path, "tile_check", [os.path.join(ROOT, "tests", "tile_check.cu")])
+
+
+def test_tensor_core_tables_and_descriptors(tmp_path):
+    _build_and_run(tmp_path, "tc_check", [os.path.join(ROOT, "tests", "tc_check.cu")])
