@@ -12,7 +12,7 @@ import ctypes
 from dataclasses import dataclass
 
 from . import _native as N
-from ._native import MOE_HAS_SHARED, MOE_HAS_SHARED_GATE, MOE_NO_FUSED, MOE_PDL  # noqa: F401
+from ._native import MOE_HAS_SHARED, MOE_HAS_SHARED_GATE, MOE_NO_FUSED, MOE_PDL, MOE_TENSOR_CORES  # noqa: F401
 
 __all__ = [
     "Dims", "MoeError", "moe_packed_expert_bytes", "moe_workspace_bytes", "moe_workspace_init",

@@ -18,6 +18,7 @@ MOE_HAS_SHARED = 1
 MOE_HAS_SHARED_GATE = 2
 MOE_NO_FUSED = 4
 MOE_PDL = 8
+MOE_TENSOR_CORES = 16
 
 # every symbol include/moe.h declares
 EXPORTS = (

@@ -6,6 +6,7 @@
 
 #include "../../include/moe.h"
 #include "moe_internal.h"
+#include "moe_tc.cuh"
 
 using namespace moe;
 
@@ -29,13 +30,17 @@ bool dims_ok(const moe_dims* d) {
   if (d->top_k < 1 || d->top_k > MOE_MAX_TOPK || d->top_k > d->n_experts) return false;
   if (d->bits != 4 && d->bits != 2) return false;
   if (!(d->rms_eps >= 0.f) || !std::isfinite(d->rms_eps)) return false;
-  if (d->flags & ~(MOE_HAS_SHARED | MOE_HAS_SHARED_GATE | MOE_NO_FUSED | MOE_PDL)) return false;
+  if (d->flags & ~(MOE_HAS_SHARED | MOE_HAS_SHARED_GATE | MOE_NO_FUSED | MOE_PDL | MOE_TENSOR_CORES)) return false;
   if ((d->flags & MOE_HAS_SHARED_GATE) && !(d->flags & MOE_HAS_SHARED)) return false;
   return true;
 }
 
 struct WsLayout {
-  size_t logits, idx, w, gs, xn, xq, xe, a, aq, ae, d, nuniq, uniq_e, uniq_off, ent, pub_logits, pub_act, total;
+  size_t logits, idx, w, gs, xn, xq, xe, a, aq, ae, d, nuniq, uniq_e, uniq_off, ent, pub_logits, pub_act;
+  // tensor-core contraction (MOE_TENSOR_CORES only): B operand rows and scales, work list
+  size_t xops, aops, xscale, ascale, chunks, nchunks;
+  int max_chunks;
+  size_t total;
 };
 
 // Byte offsets of the workspace regions for a batch of B tokens.  Only the
@@ -70,6 +75,17 @@ WsLayout ws_layout(const moe_dims& d, int B) {
   // published words of the single-token kernel (epoch << 32 | value)
   L.pub_logits = take((E + 1) * 8);
   L.pub_act = take(ns * I * 8);
+  if (d.flags & MOE_TENSOR_CORES) {
+    const size_t ne = B * ns;  // entries: (token, slot) pairs
+    L.xops = take(ne * 2 * H * 2);
+    L.aops = take(ne * 2 * I * 2);
+    L.xscale = take(ne * 4);
+    L.ascale = take(ne * 4);
+    // sum over items of ceil(n / kTcTok) <= items + entries / kTcTok
+    L.max_chunks = (int)(std::min(B * K, E) + shared_items + (ne + tc::kTcTok - 1) / tc::kTcTok);
+    L.chunks = take((size_t)L.max_chunks * sizeof(tc::TcChunk));
+    L.nchunks = take(4);
+  }
   L.total = o;
   return L;
 }
@@ -233,7 +249,7 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   cb.nslots = 1;
   cb.single = 1;
   cb.accumulate = accumulate ? 1 : 0;
-  cb.d = dn.d_out;
+  cb.d = at<float>(ws, L.d);
   cb.row_w = row_w;
   cb.out = out;
   e = launch_combine(cb, s);
@@ -262,6 +278,13 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   WsHeader* hdr = at<WsHeader>(ws, 0);
   const int shared_bits = has_shared ? layer->shared_bits : d.bits;
   cudaError_t e;
+  // The tensor-core contraction is compiled and host-checked but has not run
+  // on a GPU yet: refused until it has been validated there.
+  const bool use_tc = B > 1 && (d.flags & MOE_TENSOR_CORES);
+  if (use_tc) {
+    set_last_error("MOE_TENSOR_CORES: the tensor-core contraction is not enabled in this build");
+    return MOE_ERR_UNSUPPORTED;
+  }
 
   if (B == 1 && !(d.flags & MOE_NO_FUSED)) {
     DecodePlan plan;
@@ -349,54 +372,116 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   if ((e = launch_bucket(bk, s)) != cudaSuccess) return cuda_fail(e);
   const int items = std::min(B * K, E) + (has_shared ? (B + kSharedChunk - 1) / kSharedChunk : 0);
 
-  GateUpArgs g{};
-  g.H = H;
-  g.I = I;
-  g.K = K;
-  g.B = B;
-  g.nslots = nslots;
-  g.bits = d.bits;
-  g.shared_bits = shared_bits;
-  g.experts = static_cast<const uint8_t*>(layer->experts);
-  g.stride = layer->expert_stride;
-  g.shared = static_cast<const uint8_t*>(layer->shared);
-  g.n_uniq = bk.n_uniq;
-  g.uniq_e = bk.uniq_e;
-  g.uniq_off = bk.uniq_off;
-  g.ent = bk.ent;
-  g.xq = nq.q;
-  g.xe = nq.e;
-  g.a_out = at<float>(ws, L.a);
-  if ((e = launch_gateup(g, items, s)) != cudaSuccess) return cuda_fail(e);
+  if (use_tc) {
+    // plan -> B rows of xn -> gate/up contraction (SwiGLU) -> B rows of a -> down contraction
+    tc::TcLaunch tl{};
+    tl.H = H;
+    tl.I = I;
+    tl.E = E;
+    tl.bits = d.bits;
+    tl.shared_bits = shared_bits;
+    tl.has_shared = has_shared;
+    tl.experts = static_cast<const uint8_t*>(layer->experts);
+    tl.stride = layer->expert_stride;
+    tl.shared = static_cast<const uint8_t*>(layer->shared);
+    tl.chunks = at<tc::TcChunk>(ws, L.chunks);
+    tl.n_chunks = at<int>(ws, L.nchunks);
+    tl.max_chunks = L.max_chunks;
+    tl.ent = bk.ent;
+    tl.max_entries = B * nslots;
+    tl.xops = at<__half>(ws, L.xops);
+    tl.xscale = at<float>(ws, L.xscale);
+    tl.aops = at<__half>(ws, L.aops);
+    tl.ascale = at<float>(ws, L.ascale);
+    tl.a_out = at<float>(ws, L.a);
+    tl.d_out = at<float>(ws, L.d);
+    tl.hdr = hdr;
+    if (!tc::tc_supported(tl)) {
+      set_last_error("MOE_TENSOR_CORES: layer layout not supported by the tensor-core contraction");
+      return MOE_ERR_UNSUPPORTED;
+    }
+    tc::TcPlanArgs pl{};
+    pl.n_uniq = bk.n_uniq;
+    pl.uniq_e = bk.uniq_e;
+    pl.uniq_off = bk.uniq_off;
+    pl.bits = d.bits;
+    pl.shared_bits = shared_bits;
+    pl.chunks = at<tc::TcChunk>(ws, L.chunks);
+    pl.n_chunks = at<int>(ws, L.nchunks);
+    pl.max_chunks = L.max_chunks;
+    pl.hdr = hdr;
+    if ((e = tc::launch_tc_plan(pl, s)) != cudaSuccess) return cuda_fail(e);
+    tc::TcPackArgs px{};
+    px.src = nq.xn_out;
+    px.by_token = 1;
+    px.nslots = nslots;
+    px.K = H;
+    px.ent = bk.ent;
+    px.n_uniq = bk.n_uniq;
+    px.uniq_off = bk.uniq_off;
+    px.dst = at<__half>(ws, L.xops);
+    px.scale = at<float>(ws, L.xscale);
+    px.hdr = hdr;
+    if ((e = tc::launch_tc_pack(px, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
+    if ((e = tc::launch_tc_contract(tl, 0, s)) != cudaSuccess) return cuda_fail(e);
+    tc::TcPackArgs pa = px;
+    pa.src = tl.a_out;
+    pa.by_token = 0;
+    pa.K = I;
+    pa.dst = at<__half>(ws, L.aops);
+    pa.scale = at<float>(ws, L.ascale);
+    if ((e = tc::launch_tc_pack(pa, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
+    if ((e = tc::launch_tc_contract(tl, 1, s)) != cudaSuccess) return cuda_fail(e);
+  } else {
+    GateUpArgs g{};
+    g.H = H;
+    g.I = I;
+    g.K = K;
+    g.B = B;
+    g.nslots = nslots;
+    g.bits = d.bits;
+    g.shared_bits = shared_bits;
+    g.experts = static_cast<const uint8_t*>(layer->experts);
+    g.stride = layer->expert_stride;
+    g.shared = static_cast<const uint8_t*>(layer->shared);
+    g.n_uniq = bk.n_uniq;
+    g.uniq_e = bk.uniq_e;
+    g.uniq_off = bk.uniq_off;
+    g.ent = bk.ent;
+    g.xq = nq.q;
+    g.xe = nq.e;
+    g.a_out = at<float>(ws, L.a);
+    if ((e = launch_gateup(g, items, s)) != cudaSuccess) return cuda_fail(e);
 
-  NormQuantArgs aq{};
-  aq.in = g.a_out;
-  aq.n = I;
-  aq.do_norm = 0;
-  aq.q = at<uint8_t>(ws, L.aq);
-  aq.e = at<float2>(ws, L.ae);
-  aq.hdr = hdr;
-  if ((e = launch_norm_quant(aq, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
+    NormQuantArgs aq{};
+    aq.in = g.a_out;
+    aq.n = I;
+    aq.do_norm = 0;
+    aq.q = at<uint8_t>(ws, L.aq);
+    aq.e = at<float2>(ws, L.ae);
+    aq.hdr = hdr;
+    if ((e = launch_norm_quant(aq, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
 
-  DownArgs dn{};
-  dn.H = H;
-  dn.I = I;
-  dn.K = K;
-  dn.B = B;
-  dn.nslots = nslots;
-  dn.bits = d.bits;
-  dn.shared_bits = shared_bits;
-  dn.experts = g.experts;
-  dn.stride = g.stride;
-  dn.shared = g.shared;
-  dn.n_uniq = bk.n_uniq;
-  dn.uniq_e = bk.uniq_e;
-  dn.uniq_off = bk.uniq_off;
-  dn.ent = bk.ent;
-  dn.aq = aq.q;
-  dn.ae = aq.e;
-  dn.d_out = at<float>(ws, L.d);
-  if ((e = launch_down(dn, items, s)) != cudaSuccess) return cuda_fail(e);
+    DownArgs dn{};
+    dn.H = H;
+    dn.I = I;
+    dn.K = K;
+    dn.B = B;
+    dn.nslots = nslots;
+    dn.bits = d.bits;
+    dn.shared_bits = shared_bits;
+    dn.experts = g.experts;
+    dn.stride = g.stride;
+    dn.shared = g.shared;
+    dn.n_uniq = bk.n_uniq;
+    dn.uniq_e = bk.uniq_e;
+    dn.uniq_off = bk.uniq_off;
+    dn.ent = bk.ent;
+    dn.aq = aq.q;
+    dn.ae = aq.e;
+    dn.d_out = at<float>(ws, L.d);
+    if ((e = launch_down(dn, items, s)) != cudaSuccess) return cuda_fail(e);
+  }
 
   CombineArgs cb{};
   cb.B = B;
@@ -405,7 +490,7 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   cb.nslots = nslots;
   cb.has_shared = has_shared;
   cb.single = 0;
-  cb.d = dn.d_out;
+  cb.d = at<float>(ws, L.d);
   cb.w = t.w;
   cb.gs = t.gs;
   cb.out = h;
@@ -431,6 +516,7 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream) {
   }
   if (hh.status & ST_TIMEOUT) return MOE_ERR_TIMEOUT;
   if (hh.status & ST_NONFINITE) return MOE_ERR_NONFINITE;
+  if (hh.status & (tc::ST_RANGE | tc::ST_PLAN)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 

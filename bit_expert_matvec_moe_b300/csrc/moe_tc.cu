@@ -36,9 +36,6 @@
 namespace moe {
 namespace tc {
 
-constexpr uint32_t ST_RANGE = 4u;  // a dequantised weight outside the fp16 range of this path
-constexpr uint32_t ST_PLAN = 8u;   // more chunks than the work list holds
-
 // ---------------------------------------------------------------------------
 // work list: chunks of at most kTcTok entries per touched expert
 // ---------------------------------------------------------------------------

@@ -48,6 +48,10 @@ namespace moe {
 struct WsHeader;
 namespace tc {
 
+// status bits of this path (beside ST_TIMEOUT / ST_NONFINITE)
+constexpr uint32_t ST_RANGE = 4u;  // a dequantised weight outside the fp16 range
+constexpr uint32_t ST_PLAN = 8u;   // more chunks than the work list holds
+
 constexpr int kTcM = 128;            // weight rows per tile (MMA M)
 constexpr int kTcTok = 32;           // tokens per unit at most (MMA N = 2 * tokens <= 64)
 constexpr int kStageGroups = 8;      // groups per code stage (one TMA box = 128 bytes of codes per row)

@@ -1,0 +1,129 @@
+"""Parity of the batched tensor-core contraction (MOE_TENSOR_CORES) with the
+fp64 oracle, through moe_layer_decode.
+
+Not collected by pytest under this name: the library still refuses the flag
+(the kernels have not run on a GPU yet).  Once moe_layer_decode accepts it,
+this file becomes tests/test_gpu_tensor_cores.py.  The first case is the
+smallest one (tiny layer, B = 2, one chunk per expert), so that a first run
+exercises every kernel of the path on a few KB; the later cases cover chunks
+of more than kTcTok = 32 entries, a ragged last code stage and row tile,
+2-bit routed experts, the full-width layer with skewed routing, and equality
+of the routing with the dp4a path."""
+import numpy as np
+import pytest
+
+from synth import generate as G
+from tests.moe_testlib import REL_TOL, build_layer, rel_err, routing_ok, workspace
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import bit_expert_matvec_moe_b300 as M  # noqa: E402
+
+TINY = dict(hidden=256, inter=128, n_experts=16, top_k=4)
+FULL = dict(hidden=4096, inter=1024, n_experts=512, top_k=4)
+
+
+def D(shape, bits=4, flags=M.MOE_HAS_SHARED, **kw):
+    d = dict(shape)
+    d.update(kw)
+    return M.Dims(bits=bits, flags=flags, **d)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from bit_expert_matvec_moe_b300 import build
+    from synth import device
+
+    build.build()
+    device.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def decode_tc(L, h_np, offset=None, tc=True):
+    B = h_np.shape[0]
+    d = L.dims
+    d = M.Dims(**{**d.__dict__, "flags": d.flags | (M.MOE_TENSOR_CORES if tc else 0)})
+    layer = M.make_layer(d, L.experts, L.stride, L.router, shared=L.shared, shared_bits=L.shared_bits,
+                         rms_gamma=L.gamma, shared_gate=L.gate)
+    h = torch.from_numpy(np.ascontiguousarray(h_np, dtype=np.float32)).cuda()
+    idx = torch.empty((B, d.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((B, d.top_k), dtype=torch.float32, device="cuda")
+    off = None if offset is None else torch.from_numpy(np.ascontiguousarray(offset, dtype=np.float32)).cuda()
+    ws = workspace(d, B)
+    M.moe_layer_decode(layer, h, ws, logit_offset=off, idx_out=idx, w_out=w)
+    st = M.moe_get_device_status(ws)
+    assert st == 0, f"device status {st}"
+    return h.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def check(L, h_tok, y, idx, w, offset=None):
+    ref = L.oracle(h_tok, offset=offset)
+    ok, tie = routing_ok(idx, ref["logits"], L.dims.top_k)
+    assert ok
+    if tie:
+        ref = L.oracle(h_tok, offset=offset, force_chosen=idx)
+    assert rel_err(y, ref["y"]) <= REL_TOL, rel_err(y, ref["y"])
+    assert rel_err(y - h_tok, ref["y"] - h_tok) <= REL_TOL, rel_err(y - h_tok, ref["y"] - h_tok)
+
+
+def test_tc_tiny_two_tokens():
+    L = build_layer(D(TINY))
+    h = G.hidden_states(G.SEED, 40, 2, 256)
+    y, idx, w = decode_tc(L, h)
+    for t in range(2):
+        check(L, h[t], y[t], idx[t], w[t])
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_tc_tiny_many_tokens_per_expert(bits):
+    """33 tokens all routed to the same 4 experts: every expert (and the shared
+    one) has a chunk of 32 entries and a chunk of 1."""
+    L = build_layer(D(TINY, bits=bits), shared_bits=bits)
+    B = 33
+    h = G.hidden_states(G.SEED, 41, B, 256)
+    off = np.zeros((B, 16), np.float32)
+    off[:, [2, 5, 11, 13]] = 30.0
+    y, idx, w = decode_tc(L, h, offset=off)
+    assert all(sorted(r) == [2, 5, 11, 13] for r in idx.tolist())
+    for t in (0, 31, 32):
+        check(L, h[t], y[t], idx[t], w[t], offset=off[t])
+
+
+@pytest.mark.parametrize("variant", ["odd_shape", "no_shared", "gamma_gate"])
+def test_tc_edge_shapes(variant):
+    if variant == "odd_shape":  # 5 groups along hidden (ragged code stage), 320 down rows (ragged row tile)
+        L = build_layer(D(dict(hidden=320, inter=64, n_experts=4, top_k=2)))
+        H = 320
+    elif variant == "no_shared":
+        L = build_layer(D(TINY, flags=0))
+        H = 256
+    else:
+        L = build_layer(D(TINY, flags=M.MOE_HAS_SHARED | M.MOE_HAS_SHARED_GATE), gamma=True, shared_gate=True)
+        H = 256
+    h = G.hidden_states(G.SEED, 42, 6, H)
+    y, idx, w = decode_tc(L, h)
+    for t in (0, 5):
+        check(L, h[t], y[t], idx[t], w[t])
+
+
+@pytest.mark.parametrize("B", [8, 64])
+def test_tc_full_width_skewed(B):
+    L = build_layer(D(FULL), gen="device")
+    h = G.hidden_states(G.SEED, 43, B, 4096)
+    off = np.tile(G.popularity_offsets(G.SEED, 0, 512), (B, 1))
+    y, idx, w = decode_tc(L, h, offset=off)
+    y2, idx2, w2 = decode_tc(L, h, offset=off, tc=False)
+    assert (idx == idx2).all()  # routing does not depend on the contraction
+    assert rel_err(y, y2) <= REL_TOL
+    for t in sorted({0, B // 2, B - 1}):
+        check(L, h[t], y[t], idx[t], w[t], offset=off[t])
+
+
+def test_tc_two_bit_full_width():
+    L = build_layer(D(FULL, bits=2), gen="device")
+    h = G.hidden_states(G.SEED, 44, 8, 4096)
+    y, idx, w = decode_tc(L, h)
+    for t in (0, 7):
+        check(L, h[t], y[t], idx[t], w[t])

@@ -99,6 +99,26 @@ def test_host_validation_returns_before_launch(lib):
     assert lib.moe_workspace_init(None, 0, None) == N.MOE_ERR_INVALID_ARG
 
 
+def test_tensor_core_flag_reserved(lib):
+    """MOE_TENSOR_CORES is a valid flag: the workspace grows by the tensor-core
+    path's operand buffers (B rows of xn and of the activations, fp16 hi and lo,
+    per (token, slot) entry), and moe_layer_decode refuses it on the host for
+    B > 1 while the path is not enabled."""
+    from bit_expert_matvec_moe_b300 import _native as N
+
+    d = dims()
+    t = dims(flags=1 | N.MOE_TENSOR_CORES)
+    for B in (1, 8, 128):
+        w0 = lib.moe_workspace_bytes(ctypes.byref(d), B)
+        w1 = lib.moe_workspace_bytes(ctypes.byref(t), B)
+        entries = B * (4 + 1)
+        assert w1 - w0 >= entries * 2 * (4096 + 1024) * 2
+    layer = N.moe_layer(t, 16, 7_077_888, 32, 4, 48, None, None)
+    ws = lib.moe_workspace_bytes(ctypes.byref(t), 8)
+    assert lib.moe_layer_decode(ctypes.byref(layer), 16, 8, None, None, None, 64, ws, None) == N.MOE_ERR_UNSUPPORTED
+    assert b"MOE_TENSOR_CORES" in lib.moe_last_error_message()
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert lib.moe_status_string(s)
