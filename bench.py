@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--experts", type=int, default=512, help="routed experts (smaller pools for profiling runs)")
     p.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch between decode calls")
+    p.add_argument("--tensor-cores", action="store_true",
+                   help="B > 1: expert contractions on the tensor cores (MOE_TENSOR_CORES)")
     return p.parse_args()
 
 
@@ -202,6 +204,9 @@ def run_ours(args, rank, world, local):
     d, experts, stride, shared, router = build_full_layer(torch, M, bits=bits, n_experts=args.experts)
     if args.pdl:
         d.flags |= M.MOE_PDL
+    tc = bool(args.tensor_cores) and args.batch > 1
+    if tc:
+        d.flags |= M.MOE_TENSOR_CORES
     B = args.batch
     T = args.tokens
     nsteps_tok = T // B
@@ -313,8 +318,8 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "u4 codes x fp32 activations (int32 dp4a group sums, fp32 accumulate)" if bits == 4 else
-                 "u2 codes x fp32 activations (int32 dp4a group sums, fp32 accumulate)",
+        "dtype": (f"u{bits} codes dequantised to fp16 x fp16 hi/lo activations (tcgen05 kind::f16, fp32 accumulate)"
+                  if tc else f"u{bits} codes x fp32 activations (int32 dp4a group sums, fp32 accumulate)"),
         "data": "synthetic (seeded SplitMix64; random-init weights of the stated shape)",
         "config": {
             "workload": (f"full-width single MoE layer, batch {B}: hidden 4096, {d.n_experts} experts, top-4 routed + 1 shared, "
@@ -322,14 +327,16 @@ def run_ours(args, rank, world, local):
                          + (", per-expert popularity offsets N(0, 1.5)" if offsets is not None else "")),
             "batch": B, "tokens_per_step": T, "launches_per_step": launches_per_step,
             "l2": f"inputs larger than L2 (3.6 GB routed experts); shared expert + router rotated over {COPIES} copies",
-            "graph": graph is not None, "parallelism": f"replicas x{world}",
+            "graph": graph is not None, "parallelism": f"replicas x{world}", "tensor_cores": tc,
         },
         "expert_gbs": round(call_bytes / per_launch_s / 1e9, 1),
         "unique_experts_per_call": round(uniq, 2),
         "us_per_token": round(ms * 1e3 / T, 3),
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode_b1_kernel" if B == 1 else "gateup_kernel + down_kernel (batched path)",
+            "kernel": ("decode_b1_kernel" if B == 1 else
+                       "tc_contract_kernel, gate/up + down (batched path)" if tc else
+                       "gateup_kernel + down_kernel (batched path)"),
             "achieved": round(achieved, 1) if achieved else None,
             "peak": peak,
             "peak_kind": peak_kind,
