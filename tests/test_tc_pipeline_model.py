@@ -1,0 +1,123 @@
+"""Model check of the tensor-core contraction kernel's mbarrier protocol
+(bit_expert_matvec_moe_b300/csrc/moe_tc.cu, tc_contract_kernel): the warp
+roles are modelled as coroutines with the kernel's loop structure and its
+slot / parity arithmetic (code ring of 3, K-block ring of 4, two
+accumulators), barriers with the PTX try_wait.parity semantics and the
+kernel's arrival counts, and TMA landings and MMA commits completing in random
+order.  Every configuration must finish without a stuck wait, and every MMA
+must find the A and B blocks of its own (unit, K-block) in its slot - i.e. no
+slot is overwritten while still in use."""
+import itertools
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(s, count): s.count = count; s.pending = count; s.phase = 0; s.tx = 0
+    def arrive(s, n=1):
+        s.pending -= n
+        s._maybe()
+    def expect_tx(s, b): s.tx += b; s.arrive()
+    def complete_tx(s, b): s.tx -= b; s._maybe()
+    def _maybe(s):
+        if s.pending == 0 and s.tx == 0:
+            s.phase += 1; s.pending = s.count
+    def done(s, parity):  # try_wait.parity semantics
+        return (s.phase & 1) != parity
+
+def sim(n_units, ng, kCS=3, kKS=4, D=2, seed=0):
+    rnd = random.Random(seed)
+    nst = (ng + 7) // 8
+    full_c = [Bar(1) for _ in range(kCS)]; empty_c = [Bar(8) for _ in range(kCS)]
+    full_a = [Bar(8) for _ in range(kKS)]; full_b = [Bar(1) for _ in range(kKS)]; empty_k = [Bar(1) for _ in range(kKS)]
+    dfull = [Bar(1) for _ in range(D)]; dempty = [Bar(4) for _ in range(D)]
+    smem_c = [None]*kCS; smem_a = [None]*kKS; smem_b = [None]*kKS
+    inflight = []  # (callback) async completions (TMA, MMA commit)
+    log = {"mma": [], "epi": []}
+    def producer_codes():
+        cc = 0
+        for u in range(n_units):
+            for st in range(nst):
+                slot = cc % kCS
+                while not empty_c[slot].done(((cc // kCS) & 1) ^ 1): yield
+                full_c[slot].expect_tx(100)
+                tag = (u, st)
+                def land(slot=slot, tag=tag):
+                    smem_c[slot] = tag; full_c[slot].complete_tx(100)
+                inflight.append(land)
+                cc += 1
+    def producer_b():
+        kc = 0
+        for u in range(n_units):
+            for kb in range(ng):
+                slot = kc % kKS
+                while not empty_k[slot].done(((kc // kKS) & 1) ^ 1): yield
+                full_b[slot].expect_tx(7)
+                tag = (u, kb)
+                def land(slot=slot, tag=tag):
+                    smem_b[slot] = tag; full_b[slot].complete_tx(7)
+                inflight.append(land)
+                kc += 1
+    def mma():
+        kc = 0; uc = 0
+        for u in range(n_units):
+            d = uc & 1
+            while not dempty[d].done(((uc >> 1) & 1) ^ 1): yield
+            for kb in range(ng):
+                slot = kc % kKS; par = (kc // kKS) & 1
+                while not (full_a[slot].done(par) and full_b[slot].done(par)): yield
+                assert smem_a[slot] == (u, kb), (smem_a[slot], u, kb)
+                assert smem_b[slot] == (u, kb), (smem_b[slot], u, kb)
+                log["mma"].append((u, kb, d))
+                inflight.append(lambda slot=slot: empty_k[slot].arrive())
+                kc += 1
+            inflight.append(lambda d=d: dfull[d].arrive())
+            uc += 1
+    def epi(w):
+        uc = 0
+        for u in range(n_units):
+            d = uc & 1
+            while not dfull[d].done((uc >> 1) & 1): yield
+            if w == 0: log["epi"].append((u, d))
+            dempty[d].arrive()
+            uc += 1
+    def deq(w):
+        cc = 0; kc = 0
+        for u in range(n_units):
+            for st in range(nst):
+                cs = cc % kCS
+                while not full_c[cs].done((cc // kCS) & 1): yield
+                assert smem_c[cs] == (u, st)
+                gcount = min(8, ng - 8 * st)
+                for j in range(gcount):
+                    ks = kc % kKS
+                    while not empty_k[ks].done(((kc // kKS) & 1) ^ 1): yield
+                    smem_a[ks] = (u, 8 * st + j)
+                    full_a[ks].arrive()
+                    kc += 1
+                empty_c[cs].arrive()
+                cc += 1
+    roles = [producer_codes(), producer_b(), mma()] + [epi(i) for i in range(4)] + [deq(i) for i in range(8)]
+    alive = list(roles); idle = 0
+    while alive or inflight:
+        progressed = False
+        if inflight and rnd.random() < 0.5:
+            inflight.pop(rnd.randrange(len(inflight)))(); progressed = True
+        order = list(alive); rnd.shuffle(order)
+        for r in order:
+            try: next(r)
+            except StopIteration: alive.remove(r); progressed = True
+        if not alive and not inflight: break
+        idle = 0 if progressed else idle + 1
+        if idle > 2000 and not inflight: return False, log
+    assert len(log["mma"]) == n_units * ng and len(log["epi"]) == n_units
+    return True, log
+
+
+@pytest.mark.parametrize("n_units", [0, 1, 2, 3, 5, 9])
+@pytest.mark.parametrize("ng", [1, 2, 5, 8, 9, 16, 17, 64])
+def test_protocol_completes_and_never_overwrites_live_slots(n_units, ng):
+    for seed in range(3):
+        ok, _ = sim(n_units, ng, seed=seed)
+        assert ok, (n_units, ng, seed)
