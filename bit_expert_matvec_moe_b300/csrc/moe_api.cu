@@ -1,6 +1,7 @@
 // C ABI of the MoE decode path: argument checks, workspace layout and launches.
 // Declarations and their contract: include/moe.h.
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -396,6 +397,12 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
     tl.a_out = at<float>(ws, L.a);
     tl.d_out = at<float>(ws, L.d);
     tl.hdr = hdr;
+    // variant with the A operand in tensor memory: MOE_TC_A_IN_TMEM=1 in the environment
+    static const bool a_in_tmem = [] {
+      const char* v = std::getenv("MOE_TC_A_IN_TMEM");
+      return v && v[0] == '1';
+    }();
+    tl.a_in_tmem = a_in_tmem ? 1 : 0;
     if (!tc::tc_supported(tl)) {
       set_last_error("MOE_TENSOR_CORES: layer layout not supported by the tensor-core contraction");
       return MOE_ERR_UNSUPPORTED;

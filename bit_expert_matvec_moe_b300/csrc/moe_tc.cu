@@ -184,6 +184,10 @@ __device__ __forceinline__ void drain_ring(uint64_t* ring, int slots, uint32_t i
   for (uint32_t k = issued - n; k < issued; ++k) mbar_wait(&ring[k % slots], (k / slots) & 1u);
 }
 
+// kTmemA: the dequantised A operand goes to tensor memory (tcgen05.st, one
+// 32-column block per K slot after the accumulators) and the MMAs read it from
+// there, instead of a 128-byte-swizzled shared-memory tile.
+template <bool kTmemA>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_contract_kernel(const __grid_constant__ CUtensorMap m_codes, const __grid_constant__ CUtensorMap m_sb,
                        const __grid_constant__ CUtensorMap m_codes_sh, const __grid_constant__ CUtensorMap m_sb_sh,
@@ -229,8 +233,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tmap(&m_sb_sh);
     prefetch_tmap(&m_b);
   }
+  constexpr uint32_t kCols = kTmemA ? kTmemColsTs : kTmemCols;
   if (warp == kWarpMma) {
-    tmem_alloc(&misc[0], kTmemCols);
+    tmem_alloc(&misc[0], kCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -307,9 +312,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_after();
           const uint32_t aa = su32(sm + kOffK + slot * kKSlotBytes), ba = aa + kABytes;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ss(dt, sdesc_sw128_kmajor(aa + 32 * kk), sdesc_sw128_kmajor(ba + 32 * kk), idesc,
-                       (kb | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) {
+            if constexpr (kTmemA)
+              mma_f16_ts(dt, tmem + kTmemACol0 + slot * 32 + 8 * kk, sdesc_sw128_kmajor(ba + 32 * kk), idesc,
+                         (kb | kk) != 0);
+            else
+              mma_f16_ss(dt, sdesc_sw128_kmajor(aa + 32 * kk), sdesc_sw128_kmajor(ba + 32 * kk), idesc,
+                         (kb | kk) != 0);
+          }
           mma_commit(&empty_k[slot]);
         }
         if (ok) mma_commit(&dfull[d]);
@@ -380,27 +390,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (j >= gcount) break;
           const uint32_t ks = kc % kKSlots;
           if (!(ok = tc_wait_warp(&empty_k[ks], ((kc / kKSlots) & 1u) ^ 1u, abort))) break;
-          uint8_t* A = sm + kOffK + ks * kKSlotBytes;
           const float s = bf16lo(sbw[j]), b = bf16hi(sbw[j]);
           bad |= !(fabsf(s) * qmax + fabsf(b) <= 65504.f);
           const __half2 s2 = __float2half2_rn(s), b2 = __float2half2_rn(b);
+          uint4 c0, c1, c2, c3;  // chunks 4h .. 4h+3 of this row's K-block
           if (ch.bits == 4) {
             const uint4 c = *reinterpret_cast<const uint4*>(cb + h * kHalfBoxBytes + swz128(r, j));
-            *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 0)) = dequant_word4(c.x, s2, b2);
-            *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 1)) = dequant_word4(c.y, s2, b2);
-            *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 2)) = dequant_word4(c.z, s2, b2);
-            *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 3)) = dequant_word4(c.w, s2, b2);
+            c0 = dequant_word4(c.x, s2, b2);
+            c1 = dequant_word4(c.y, s2, b2);
+            c2 = dequant_word4(c.z, s2, b2);
+            c3 = dequant_word4(c.w, s2, b2);
           } else {
             const uint2 c = *reinterpret_cast<const uint2*>(cb + swz128(r, j) + 8 * h);
-            uint4 c0, c1, c2, c3;
             dequant_word2(c.x, s2, b2, c0, c1);
             dequant_word2(c.y, s2, b2, c2, c3);
+          }
+          if constexpr (kTmemA) {
+            // lane r of the tile, 16 columns = this half's 32 inputs
+            const uint32_t v[16] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w,
+                                    c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w};
+            tc_fence_after();  // the MMAs that read this slot have completed (empty_k)
+            tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + kTmemACol0 + ks * 32 + 16 * h, v);
+            tmem_st_wait();
+            tc_fence_before();
+          } else {
+            uint8_t* A = sm + kOffK + ks * kKSlotBytes;
             *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 0)) = c0;
             *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 1)) = c1;
             *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 2)) = c2;
             *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 3)) = c3;
+            fence_proxy_async();  // generic-proxy writes -> visible to the MMA (async proxy)
           }
-          fence_proxy_async();  // generic-proxy writes -> visible to the MMA (async proxy)
           __syncwarp();
           if (lane == 0) mbar_arrive(&full_a[ks]);
           ++kc;
@@ -418,7 +438,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == kWarpMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, kCols);
   }
   if (threadIdx.x == 0) {
     const uint32_t st = misc[2] | (*abort ? (uint32_t)ST_TIMEOUT : 0u);
@@ -525,7 +545,9 @@ cudaError_t launch_tc_contract(const TcLaunch& L, int mode, cudaStream_t s) {
   a.bscale = gu ? L.xscale : L.ascale;
   a.out = gu ? L.a_out : L.d_out;
   a.hdr = L.hdr;
-  cudaError_t e = ensure_dynamic_smem(tc_contract_kernel, (int)kSmemBytes, configured);
+  static std::atomic<int> configured_ts[kMaxDevices];
+  cudaError_t e = L.a_in_tmem ? ensure_dynamic_smem(tc_contract_kernel<true>, (int)kSmemBytes, configured_ts)
+                              : ensure_dynamic_smem(tc_contract_kernel<false>, (int)kSmemBytes, configured);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -533,7 +555,10 @@ cudaError_t launch_tc_contract(const TcLaunch& L, int mode, cudaStream_t s) {
   const long long max_units = (long long)L.max_chunks * a.tiles;
   const int grid = (int)(max_units < sms ? max_units : sms);
   if (grid <= 0) return cudaSuccess;
-  tc_contract_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(mc, ms, mcs, mss, mb, a);
+  if (L.a_in_tmem)
+    tc_contract_kernel<true><<<grid, kTcThreads, kSmemBytes, s>>>(mc, ms, mcs, mss, mb, a);
+  else
+    tc_contract_kernel<false><<<grid, kTcThreads, kSmemBytes, s>>>(mc, ms, mcs, mss, mb, a);
   return cudaGetLastError();
 }
 

@@ -121,6 +121,21 @@ def test_tc_full_width_skewed(B):
         check(L, h[t], y[t], idx[t], w[t], offset=off[t])
 
 
+def test_tc_a_in_tensor_memory_variant():
+    """The A-in-tensor-memory variant (MOE_TC_A_IN_TMEM=1, read once per
+    process) on the tiny and the full-width layer, in a child process."""
+    import os
+    import subprocess
+    import sys
+
+    code = ("import tests.pending_gpu_tensor_cores as T; T.test_tc_tiny_two_tokens(); "
+            "T.test_tc_tiny_many_tokens_per_expert(4); T.test_tc_full_width_skewed(8)")
+    env = dict(os.environ, MOE_TC_A_IN_TMEM="1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+
+
 def test_tc_two_bit_full_width():
     L = build_layer(D(FULL, bits=2), gen="device")
     h = G.hidden_states(G.SEED, 44, 8, 4096)
