@@ -353,6 +353,10 @@ def run_ours(args, rank, world, local):
     print(f"# {tok_s:.1f} tokens/s, {ms * 1e3 / T:.3f} us/token, e2e {e2e:.3f} ms/step", file=sys.stderr, flush=True)
     if rank == 0 and args.config == 2 and B == 1 and args.cpu_seconds > 0:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        ncpu = os.cpu_count() or 1
+        if ncpu > 1:  # the same oracle with its BLAS on every host core
+            mt = cpu_baseline(args.cpu_seconds / 2, threads=ncpu)
+            out["cpu_baseline"]["all_cores"] = {"value": mt["value"], "cores": mt["cores"], "sample": mt["sample"]}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -504,19 +508,20 @@ def run_stack(args, rank, world, local):
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) timing
-def cpu_baseline(seconds: float, tokens_max: int = 64):
-    """The fp64 oracle as it stands, one thread, on a bounded sample of the same
-    workload, run in a child process whose BLAS is pinned to one thread."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
+def cpu_baseline(seconds: float, tokens_max: int = 64, threads: int = 1):
+    """The fp64 oracle as it stands on a bounded sample of the same workload,
+    run in a child process whose BLAS uses `threads` threads (1: one core; the
+    oracle's matvecs are the only multi-threaded part)."""
+    t = str(threads)
+    env = dict(os.environ, OMP_NUM_THREADS=t, OPENBLAS_NUM_THREADS=t, MKL_NUM_THREADS=t, CUDA_VISIBLE_DEVICES="")
     res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", str(seconds),
-                          str(tokens_max)], capture_output=True, text=True, env=env, timeout=600)
+                          str(tokens_max), t], capture_output=True, text=True, env=env, timeout=600)
     if res.returncode != 0:
         raise RuntimeError("oracle timing failed: " + res.stderr[-2000:])
     return json.loads(res.stdout.strip().splitlines()[-1])
 
 
-def _cpu_baseline_child(seconds: float, tokens_max: int):
+def _cpu_baseline_child(seconds: float, tokens_max: int, threads: int = 1):
     """Tokens are decoded one by one until `seconds` of oracle time pass.  The
     touched experts are generated before each token's timing (input generation
     is not oracle work)."""
@@ -543,8 +548,9 @@ def _cpu_baseline_child(seconds: float, tokens_max: int):
         O.layer_decode(h[done], experts=get, shared=shared, router_bits=R, top_k=K, hidden=H, inter=I)
         spent += time.perf_counter() - t0
         done += 1
-    return {"value": round(done / spent, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} of the {TOKENS} decode tokens of the same layer, fp64 numpy, 1 thread"}
+    return {"value": round(done / spent, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} of the {TOKENS} decode tokens of the same layer, fp64 numpy, "
+                      f"{threads} BLAS thread{'s' if threads > 1 else ''}"}
 
 
 def run_reference(args, rank, world):
@@ -585,8 +591,8 @@ def run_reference(args, rank, world):
 
 
 def main():
-    if len(sys.argv) == 4 and sys.argv[1] == "--cpu-baseline-child":
-        print(json.dumps(_cpu_baseline_child(float(sys.argv[2]), int(sys.argv[3]))))
+    if len(sys.argv) == 5 and sys.argv[1] == "--cpu-baseline-child":
+        print(json.dumps(_cpu_baseline_child(float(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4]))))
         return
     args = parse()
     rank, world, local = dist_env()
