@@ -426,6 +426,7 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
     px.ent = bk.ent;
     px.n_uniq = bk.n_uniq;
     px.uniq_off = bk.uniq_off;
+    px.n_ids = B * nslots;
     px.dst = at<__half>(ws, L.xops);
     px.scale = at<float>(ws, L.xscale);
     px.hdr = hdr;
@@ -523,7 +524,7 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream) {
   }
   if (hh.status & ST_TIMEOUT) return MOE_ERR_TIMEOUT;
   if (hh.status & ST_NONFINITE) return MOE_ERR_NONFINITE;
-  if (hh.status & (tc::ST_RANGE | tc::ST_PLAN)) return MOE_ERR_UNSUPPORTED;
+  if (hh.status & (tc::ST_RANGE | tc::ST_PLAN | tc::ST_BOUNDS)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 

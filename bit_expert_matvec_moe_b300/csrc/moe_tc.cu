@@ -84,6 +84,10 @@ __global__ void __launch_bounds__(256) tc_pack_kernel(TcPackArgs a) {
   const int total = a.uniq_off[*a.n_uniq];
   if (j >= total) return;
   const int id = a.ent[j];
+  if (id < 0 || id >= a.n_ids) {  // cannot happen with a consistent work list
+    if (threadIdx.x == 0) atomicOr(&a.hdr->status, ST_BOUNDS);
+    return;
+  }
   const float* src = a.src + (size_t)(a.by_token ? id / a.nslots : id) * a.K;
   __shared__ float red[8];
   float m = 0.f;
@@ -356,8 +360,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int t = 8 * cb + i;
           if (t < ch.n) {
             const int j = ch.e0 + t;
+            const int id = (j >= 0 && j < a.max_entries) ? a.ent[j] : -1;
+            if (id < 0 || id >= a.n_ids) {  // cannot happen with a consistent work list
+              if (lane == 0) atomicOr(&misc[2], ST_BOUNDS);
+              continue;
+            }
             const float val = (__uint_as_float(v[cb][2 * i]) + __uint_as_float(v[cb][2 * i + 1])) * a.bscale[j];
-            const size_t o = (size_t)a.ent[j] * a.out_cols;
+            const size_t o = (size_t)id * a.out_cols;
             if (a.mode == 0) {
               const float up = __shfl_xor_sync(0xffffffffu, val, 1);  // rows 2p (gate) and 2p + 1 (up)
               if (!(lane & 1) && row < a.rows) a.out[o + (row >> 1)] = silu_mul(val, up);
@@ -544,6 +553,8 @@ cudaError_t launch_tc_contract(const TcLaunch& L, int mode, cudaStream_t s) {
   a.ent = L.ent;
   a.bscale = gu ? L.xscale : L.ascale;
   a.out = gu ? L.a_out : L.d_out;
+  a.max_entries = L.max_entries;
+  a.n_ids = L.max_entries;
   a.hdr = L.hdr;
   static std::atomic<int> configured_ts[kMaxDevices];
   cudaError_t e = L.a_in_tmem ? ensure_dynamic_smem(tc_contract_kernel<true>, (int)kSmemBytes, configured_ts)

@@ -51,6 +51,7 @@ namespace tc {
 // status bits of this path (beside ST_TIMEOUT / ST_NONFINITE)
 constexpr uint32_t ST_RANGE = 4u;  // a dequantised weight outside the fp16 range
 constexpr uint32_t ST_PLAN = 8u;   // more chunks than the work list holds
+constexpr uint32_t ST_BOUNDS = 16u;  // an entry or (token, slot) id outside its buffer (access skipped)
 
 constexpr int kTcM = 128;            // weight rows per tile (MMA M)
 constexpr int kTcTok = 32;           // tokens per unit at most (MMA N = 2 * tokens <= 64)
@@ -288,6 +289,7 @@ struct TcPackArgs {
   const int* ent;       // entry -> token * nslots + slot
   const int* n_uniq;
   const int* uniq_off;
+  int n_ids;            // batch * nslots: (token, slot) ids
   __half* dst;          // [entries * 2][K]: hi row, lo row
   float* scale;         // [entries]: 2^e
   WsHeader* hdr;
@@ -305,6 +307,8 @@ struct TcContractArgs {
   const int* ent;
   const float* bscale;  // [entries] scale of the B rows
   float* out;           // [(token, slot) id][out_cols]
+  int max_entries;      // size of ent / bscale
+  int n_ids;            // rows of out: batch * slots
   WsHeader* hdr;
 };
 

@@ -204,6 +204,9 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B,
  * Synchronise `stream`, read the workspace status word, clear it and return
  * it (MOE_OK when no device-side error was recorded).  After a device-side
  * error the kernels of later calls return early until the status is cleared.
+ * MOE_ERR_TIMEOUT: a bounded device wait ran out; MOE_ERR_NONFINITE: a
+ * non-finite activation; MOE_ERR_UNSUPPORTED: the tensor-core contraction met
+ * a weight outside the fp16 range or an inconsistent work list.
  */
 moe_status moe_get_device_status(void* ws, moe_stream_t stream);
 
