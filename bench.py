@@ -351,10 +351,11 @@ def run_ours(args, rank, world, local):
         "clocks": ck,
     }
     print(f"# {tok_s:.1f} tokens/s, {ms * 1e3 / T:.3f} us/token, e2e {e2e:.3f} ms/step", file=sys.stderr, flush=True)
-    if rank == 0 and args.config == 2 and B == 1 and args.cpu_seconds > 0:
-        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0 and args.cpu_seconds > 0:
+        # the oracle decodes token by token: batching does not change its tokens/s
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, bits=bits)
         ncpu = os.cpu_count() or 1
-        if ncpu > 1:  # the same oracle with its BLAS on every host core
+        if ncpu > 1 and args.config == 2 and B == 1:  # the same oracle with its BLAS on every host core
             mt = cpu_baseline(args.cpu_seconds / 2, threads=ncpu)
             out["cpu_baseline"]["all_cores"] = {"value": mt["value"], "cores": mt["cores"], "sample": mt["sample"]}
     if rank == 0:
@@ -501,6 +502,11 @@ def run_stack(args, rank, world, local):
         "clocks": ck,
     }
     print(f"# {tok_s:.1f} tokens/s through {Lyr} layers, {per_launch_s * 1e6:.3f} us/layer", file=sys.stderr, flush=True)
+    if rank == 0 and args.cpu_seconds > 0:
+        # one token through the stack = Lyr single-layer decodes of the same shape for the oracle
+        cb = cpu_baseline(args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(cb["value"] / Lyr, 5), "unit": "tokens/s", "cores": cb["cores"],
+                               "kind": "oracle", "sample": cb["sample"] + f"; extrapolated x{Lyr} layers per token"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -508,20 +514,20 @@ def run_stack(args, rank, world, local):
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) timing
-def cpu_baseline(seconds: float, tokens_max: int = 64, threads: int = 1):
+def cpu_baseline(seconds: float, tokens_max: int = 64, threads: int = 1, bits: int = 4):
     """The fp64 oracle as it stands on a bounded sample of the same workload,
     run in a child process whose BLAS uses `threads` threads (1: one core; the
     oracle's matvecs are the only multi-threaded part)."""
     t = str(threads)
     env = dict(os.environ, OMP_NUM_THREADS=t, OPENBLAS_NUM_THREADS=t, MKL_NUM_THREADS=t, CUDA_VISIBLE_DEVICES="")
     res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", str(seconds),
-                          str(tokens_max), t], capture_output=True, text=True, env=env, timeout=600)
+                          str(tokens_max), t, str(bits)], capture_output=True, text=True, env=env, timeout=600)
     if res.returncode != 0:
         raise RuntimeError("oracle timing failed: " + res.stderr[-2000:])
     return json.loads(res.stdout.strip().splitlines()[-1])
 
 
-def _cpu_baseline_child(seconds: float, tokens_max: int, threads: int = 1):
+def _cpu_baseline_child(seconds: float, tokens_max: int, threads: int = 1, bits: int = 4):
     """Tokens are decoded one by one until `seconds` of oracle time pass.  The
     touched experts are generated before each token's timing (input generation
     is not oracle work)."""
@@ -536,7 +542,7 @@ def _cpu_baseline_child(seconds: float, tokens_max: int, threads: int = 1):
 
     def get(e):
         if e not in cache:
-            cache[e] = G.expert(G.SEED, 0, e, H, I, 4)
+            cache[e] = G.expert(G.SEED, 0, e, H, I, bits)
         return cache[e]
 
     done, spent = 0, 0.0
@@ -549,7 +555,7 @@ def _cpu_baseline_child(seconds: float, tokens_max: int, threads: int = 1):
         spent += time.perf_counter() - t0
         done += 1
     return {"value": round(done / spent, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{done} of the {TOKENS} decode tokens of the same layer, fp64 numpy, "
+            "sample": f"{done} of the {TOKENS} decode tokens of the same layer ({bits}-bit routed experts), fp64 numpy, "
                       f"{threads} BLAS thread{'s' if threads > 1 else ''}"}
 
 
@@ -591,8 +597,8 @@ def run_reference(args, rank, world):
 
 
 def main():
-    if len(sys.argv) == 5 and sys.argv[1] == "--cpu-baseline-child":
-        print(json.dumps(_cpu_baseline_child(float(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4]))))
+    if len(sys.argv) == 6 and sys.argv[1] == "--cpu-baseline-child":
+        print(json.dumps(_cpu_baseline_child(float(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5]))))
         return
     args = parse()
     rank, world, local = dist_env()
