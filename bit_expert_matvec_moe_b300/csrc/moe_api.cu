@@ -102,6 +102,89 @@ int current_device() {
   return dev;
 }
 
+// The tensor-core contraction of a bucketed work list: plan (chunks of at
+// most 32 entries) -> B rows of xn -> gate/up contraction with SwiGLU -> B
+// rows of the activations -> down contraction into the workspace's d rows.
+struct TcSource {
+  const uint8_t* experts;
+  size_t stride;
+  int E, bits;
+  const uint8_t* shared;
+  int shared_bits, has_shared;
+  const float* xn;  // [tokens][H]
+};
+moe_status run_tc(const moe_dims& d, const WsLayout& L, void* ws, int B, int nslots, const TcSource& src,
+                  int* n_uniq, int* uniq_e, int* uniq_off, int* ent, cudaStream_t s) {
+  WsHeader* hdr = at<WsHeader>(ws, 0);
+  tc::TcLaunch tl{};
+  tl.H = d.hidden;
+  tl.I = d.inter;
+  tl.E = src.E;
+  tl.bits = src.bits;
+  tl.shared_bits = src.shared_bits;
+  tl.has_shared = src.has_shared;
+  tl.experts = src.experts;
+  tl.stride = src.stride;
+  tl.shared = src.shared;
+  tl.chunks = at<tc::TcChunk>(ws, L.chunks);
+  tl.n_chunks = at<int>(ws, L.nchunks);
+  tl.max_chunks = L.max_chunks;
+  tl.ent = ent;
+  tl.max_entries = B * nslots;
+  tl.xops = at<__half>(ws, L.xops);
+  tl.xscale = at<float>(ws, L.xscale);
+  tl.aops = at<__half>(ws, L.aops);
+  tl.ascale = at<float>(ws, L.ascale);
+  tl.a_out = at<float>(ws, L.a);
+  tl.d_out = at<float>(ws, L.d);
+  tl.hdr = hdr;
+  // variant with the A operand in tensor memory: MOE_TC_A_IN_TMEM=1 in the environment
+  static const bool a_in_tmem = [] {
+    const char* v = std::getenv("MOE_TC_A_IN_TMEM");
+    return v && v[0] == '1';
+  }();
+  tl.a_in_tmem = a_in_tmem ? 1 : 0;
+  if (!tc::tc_supported(tl)) {
+    set_last_error("MOE_TENSOR_CORES: layer layout not supported by the tensor-core contraction");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  cudaError_t e;
+  tc::TcPlanArgs pl{};
+  pl.n_uniq = n_uniq;
+  pl.uniq_e = uniq_e;
+  pl.uniq_off = uniq_off;
+  pl.bits = src.bits;
+  pl.shared_bits = src.shared_bits;
+  pl.chunks = at<tc::TcChunk>(ws, L.chunks);
+  pl.n_chunks = at<int>(ws, L.nchunks);
+  pl.max_chunks = L.max_chunks;
+  pl.hdr = hdr;
+  if ((e = tc::launch_tc_plan(pl, s)) != cudaSuccess) return cuda_fail(e);
+  tc::TcPackArgs px{};
+  px.src = src.xn;
+  px.by_token = 1;
+  px.nslots = nslots;
+  px.K = d.hidden;
+  px.ent = ent;
+  px.n_uniq = n_uniq;
+  px.uniq_off = uniq_off;
+  px.n_ids = B * nslots;
+  px.dst = at<__half>(ws, L.xops);
+  px.scale = at<float>(ws, L.xscale);
+  px.hdr = hdr;
+  if ((e = tc::launch_tc_pack(px, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = tc::launch_tc_contract(tl, 0, s)) != cudaSuccess) return cuda_fail(e);
+  tc::TcPackArgs pa = px;
+  pa.src = tl.a_out;
+  pa.by_token = 0;
+  pa.K = d.inter;
+  pa.dst = at<__half>(ws, L.aops);
+  pa.scale = at<float>(ws, L.ascale);
+  if ((e = tc::launch_tc_pack(pa, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = tc::launch_tc_contract(tl, 1, s)) != cudaSuccess) return cuda_fail(e);
+  return MOE_OK;
+}
+
 }  // namespace
 
 namespace moe {
@@ -195,6 +278,43 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int H = dims->hidden, I = dims->inter;
   WsHeader* hdr = at<WsHeader>(ws, 0);
+  if (B > 1 && (dims->flags & MOE_TENSOR_CORES)) {
+    // not enabled until validated on the GPU (as in moe_layer_decode)
+    set_last_error("MOE_TENSOR_CORES: the tensor-core contraction is not enabled in this build");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (B > 1 && (dims->flags & MOE_TENSOR_CORES)) {
+    // one expert for tokens 0 .. B-1: a single work item through the shared-expert maps
+    const size_t blob_bytes = make_fmt(bits, H, I).total;
+    cudaError_t e = tc::launch_tc_single_item(B, at<int>(ws, L.nuniq), at<int>(ws, L.uniq_e), at<int>(ws, L.uniq_off),
+                                              at<int>(ws, L.ent), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    TcSource src{};
+    src.experts = static_cast<const uint8_t*>(blob);
+    src.stride = blob_bytes;
+    src.E = 1;
+    src.bits = bits;
+    src.shared = static_cast<const uint8_t*>(blob);
+    src.shared_bits = bits;
+    src.has_shared = 1;
+    src.xn = xn;
+    const moe_status st =
+        run_tc(*dims, L, ws, B, 1, src, at<int>(ws, L.nuniq), at<int>(ws, L.uniq_e), at<int>(ws, L.uniq_off),
+               at<int>(ws, L.ent), s);
+    if (st != MOE_OK) return st;
+    CombineArgs cb{};
+    cb.B = B;
+    cb.H = H;
+    cb.K = 0;
+    cb.nslots = 1;
+    cb.single = 1;
+    cb.accumulate = accumulate ? 1 : 0;
+    cb.d = at<float>(ws, L.d);
+    cb.row_w = row_w;
+    cb.out = out;
+    e = launch_combine(cb, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+  }
   NormQuantArgs nq{};
   nq.in = xn;
   nq.n = H;
@@ -374,72 +494,17 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   const int items = std::min(B * K, E) + (has_shared ? (B + kSharedChunk - 1) / kSharedChunk : 0);
 
   if (use_tc) {
-    // plan -> B rows of xn -> gate/up contraction (SwiGLU) -> B rows of a -> down contraction
-    tc::TcLaunch tl{};
-    tl.H = H;
-    tl.I = I;
-    tl.E = E;
-    tl.bits = d.bits;
-    tl.shared_bits = shared_bits;
-    tl.has_shared = has_shared;
-    tl.experts = static_cast<const uint8_t*>(layer->experts);
-    tl.stride = layer->expert_stride;
-    tl.shared = static_cast<const uint8_t*>(layer->shared);
-    tl.chunks = at<tc::TcChunk>(ws, L.chunks);
-    tl.n_chunks = at<int>(ws, L.nchunks);
-    tl.max_chunks = L.max_chunks;
-    tl.ent = bk.ent;
-    tl.max_entries = B * nslots;
-    tl.xops = at<__half>(ws, L.xops);
-    tl.xscale = at<float>(ws, L.xscale);
-    tl.aops = at<__half>(ws, L.aops);
-    tl.ascale = at<float>(ws, L.ascale);
-    tl.a_out = at<float>(ws, L.a);
-    tl.d_out = at<float>(ws, L.d);
-    tl.hdr = hdr;
-    // variant with the A operand in tensor memory: MOE_TC_A_IN_TMEM=1 in the environment
-    static const bool a_in_tmem = [] {
-      const char* v = std::getenv("MOE_TC_A_IN_TMEM");
-      return v && v[0] == '1';
-    }();
-    tl.a_in_tmem = a_in_tmem ? 1 : 0;
-    if (!tc::tc_supported(tl)) {
-      set_last_error("MOE_TENSOR_CORES: layer layout not supported by the tensor-core contraction");
-      return MOE_ERR_UNSUPPORTED;
-    }
-    tc::TcPlanArgs pl{};
-    pl.n_uniq = bk.n_uniq;
-    pl.uniq_e = bk.uniq_e;
-    pl.uniq_off = bk.uniq_off;
-    pl.bits = d.bits;
-    pl.shared_bits = shared_bits;
-    pl.chunks = at<tc::TcChunk>(ws, L.chunks);
-    pl.n_chunks = at<int>(ws, L.nchunks);
-    pl.max_chunks = L.max_chunks;
-    pl.hdr = hdr;
-    if ((e = tc::launch_tc_plan(pl, s)) != cudaSuccess) return cuda_fail(e);
-    tc::TcPackArgs px{};
-    px.src = nq.xn_out;
-    px.by_token = 1;
-    px.nslots = nslots;
-    px.K = H;
-    px.ent = bk.ent;
-    px.n_uniq = bk.n_uniq;
-    px.uniq_off = bk.uniq_off;
-    px.n_ids = B * nslots;
-    px.dst = at<__half>(ws, L.xops);
-    px.scale = at<float>(ws, L.xscale);
-    px.hdr = hdr;
-    if ((e = tc::launch_tc_pack(px, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
-    if ((e = tc::launch_tc_contract(tl, 0, s)) != cudaSuccess) return cuda_fail(e);
-    tc::TcPackArgs pa = px;
-    pa.src = tl.a_out;
-    pa.by_token = 0;
-    pa.K = I;
-    pa.dst = at<__half>(ws, L.aops);
-    pa.scale = at<float>(ws, L.ascale);
-    if ((e = tc::launch_tc_pack(pa, B * nslots, s)) != cudaSuccess) return cuda_fail(e);
-    if ((e = tc::launch_tc_contract(tl, 1, s)) != cudaSuccess) return cuda_fail(e);
+    TcSource src{};
+    src.experts = static_cast<const uint8_t*>(layer->experts);
+    src.stride = layer->expert_stride;
+    src.E = E;
+    src.bits = d.bits;
+    src.shared = static_cast<const uint8_t*>(layer->shared);
+    src.shared_bits = shared_bits;
+    src.has_shared = has_shared;
+    src.xn = nq.xn_out;
+    const moe_status st = run_tc(d, L, ws, B, nslots, src, bk.n_uniq, bk.uniq_e, bk.uniq_off, bk.ent, s);
+    if (st != MOE_OK) return st;
   } else {
     GateUpArgs g{};
     g.H = H;

@@ -76,6 +76,18 @@ __global__ void __launch_bounds__(32) tc_plan_kernel(TcPlanArgs a) {
   if (lane == 0) *a.n_chunks = min(total, a.max_chunks);
 }
 
+// Work list of one expert applied to tokens 0 .. B-1 (moe_expert_forward): a
+// single item, taken through the shared-expert tensor maps.
+__global__ void tc_single_item_kernel(int B, int* n_uniq, int* uniq_e, int* uniq_off, int* ent) {
+  for (int j = threadIdx.x; j < B; j += blockDim.x) ent[j] = j;
+  if (threadIdx.x == 0) {
+    *n_uniq = 1;
+    uniq_e[0] = -1;
+    uniq_off[0] = 0;
+    uniq_off[1] = B;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // B operand rows: fp16 hi / lo of each entry's activation, scaled per entry
 // ---------------------------------------------------------------------------
@@ -512,6 +524,11 @@ bool tc_supported(const TcLaunch& L) {
   if (L.has_shared && L.shared_bits != 4 && L.shared_bits != 2) return false;
   if (!al16(L.experts) || (L.stride & 15u) || (L.has_shared && !al16(L.shared))) return false;
   return encode_fn() != nullptr;
+}
+
+cudaError_t launch_tc_single_item(int B, int* n_uniq, int* uniq_e, int* uniq_off, int* ent, cudaStream_t s) {
+  tc_single_item_kernel<<<1, 256, 0, s>>>(B, n_uniq, uniq_e, uniq_off, ent);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tc_plan(const TcPlanArgs& a, cudaStream_t s) {

@@ -335,6 +335,7 @@ struct TcLaunch {
   int a_in_tmem;           // A operand in tensor memory (tcgen05.st) instead of shared memory
 };
 bool tc_supported(const TcLaunch& L);
+cudaError_t launch_tc_single_item(int B, int* n_uniq, int* uniq_e, int* uniq_off, int* ent, cudaStream_t s);
 cudaError_t launch_tc_plan(const TcPlanArgs& a, cudaStream_t s);
 cudaError_t launch_tc_pack(const TcPackArgs& a, int max_entries, cudaStream_t s);
 cudaError_t launch_tc_contract(const TcLaunch& L, int mode, cudaStream_t s);

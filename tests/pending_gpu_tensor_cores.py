@@ -3,9 +3,9 @@ fp64 oracle, through moe_layer_decode.
 
 Not collected by pytest under this name: the library still refuses the flag
 (the kernels have not run on a GPU yet).  Once moe_layer_decode accepts it,
-this file becomes tests/test_gpu_tensor_cores.py.  The first case is the
-smallest one (tiny layer, B = 2, one chunk per expert), so that a first run
-exercises every kernel of the path on a few KB; the later cases cover chunks
+this file becomes tests/test_gpu_tensor_cores.py.  The first cases run
+one expert through moe_expert_forward (tiny shape first: a few KB, every
+kernel of the path once), then the tiny layer at B = 2; the later cases cover chunks
 of more than kTcTok = 32 entries, a ragged last code stage and row tile,
 2-bit routed experts, the full-width layer with skewed routing, and equality
 of the routing with the dp4a path."""
@@ -66,6 +66,36 @@ def check(L, h_tok, y, idx, w, offset=None):
         ref = L.oracle(h_tok, offset=offset, force_chosen=idx)
     assert rel_err(y, ref["y"]) <= REL_TOL, rel_err(y, ref["y"])
     assert rel_err(y - h_tok, ref["y"] - h_tok) <= REL_TOL, rel_err(y - h_tok, ref["y"] - h_tok)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("shape", [TINY, FULL, dict(hidden=320, inter=64, n_experts=4, top_k=2)])
+def test_tc_expert_forward(bits, shape):
+    """One expert on B = 3 tokens through moe_expert_forward: each token's
+    expert output against the oracle, overwrite and weighted accumulate."""
+    from oracle import moe_oracle as O
+    from tests.moe_testlib import pack_expert_device
+
+    d = D(shape, bits=bits, flags=M.MOE_TENSOR_CORES)
+    H, I, B = d.hidden, d.inter, 3
+    canon = G.expert(G.SEED, 2, 9, H, I, bits)
+    blob = torch.empty(M.moe_packed_expert_bytes(d, bits), dtype=torch.uint8, device="cuda")
+    pack_expert_device(d, bits, canon, blob, torch)
+    xn = G.hidden_states(G.SEED, 2, B, H)
+    base = G.hidden_states(G.SEED, 3, B, H)
+    row_w = np.array([0.5, -1.25, 2.0], np.float32)
+    ws = workspace(d, B)
+    out = torch.from_numpy(base.copy()).cuda()
+    M.moe_expert_forward(d, bits, blob, torch.from_numpy(xn).cuda(), out, ws,
+                         row_w=torch.from_numpy(row_w).cuda(), accumulate=True)
+    out2 = torch.zeros((B, H), dtype=torch.float32, device="cuda")
+    M.moe_expert_forward(d, bits, blob, torch.from_numpy(xn).cuda(), out2, ws)
+    assert M.moe_get_device_status(ws) == 0
+    out, out2 = out.cpu().numpy(), out2.cpu().numpy()
+    for b in range(B):
+        ref = O.expert_forward(canon, xn[b], H, I)["d"]
+        assert rel_err(out2[b], ref) <= REL_TOL, rel_err(out2[b], ref)
+        assert rel_err(out[b], base[b] + row_w[b] * ref) <= REL_TOL
 
 
 def test_tc_tiny_two_tokens():

@@ -117,6 +117,8 @@ def test_tensor_core_flag_reserved(lib):
     ws = lib.moe_workspace_bytes(ctypes.byref(t), 8)
     assert lib.moe_layer_decode(ctypes.byref(layer), 16, 8, None, None, None, 64, ws, None) == N.MOE_ERR_UNSUPPORTED
     assert b"MOE_TENSOR_CORES" in lib.moe_last_error_message()
+    # moe_expert_forward refuses it the same way for B > 1
+    assert lib.moe_expert_forward(ctypes.byref(t), 4, 16, 32, 3, None, 48, 0, 64, ws, None) == N.MOE_ERR_UNSUPPORTED
 
 
 def test_status_strings(lib):
