@@ -13,6 +13,8 @@ _orig_rms = O.rmsnorm
 _orig_rw = O.routing_weights
 _orig_silu = O.silu
 _orig_router = O.router_logits
+_orig_expert = O.expert_forward
+_orig_layer = O.layer_decode
 
 
 def _dequant_no_bias(codes, scales, biases, bits, group, n):
@@ -59,6 +61,34 @@ def _topk_high_index_ties(logits, k):
     return order[:k]
 
 
+def _expert_silu_on_up(ex, xn, hidden, inter):
+    out = _orig_expert(ex, xn, hidden, inter)
+    a = O.silu(out["u"]) * out["g"]
+    wd = O.dequant(*ex["down"], ex["bits"], ex["group"], inter)
+    return {**out, "a": a, "d": wd @ a}
+
+
+def _shared_gate_swapped(out, g_new):
+    if "d_shared" not in out:
+        return out
+    y = out["y"] + (g_new - out["g_shared"]) * out["d_shared"]
+    return {**out, "y": y, "g_shared": g_new}
+
+
+def _layer_gate_sign(h, **kw):
+    out = _orig_layer(h, **kw)
+    if kw.get("shared_gate_bits") is None:
+        return out
+    return _shared_gate_swapped(out, 1.0 - out["g_shared"])  # sigmoid(-t) = 1 - sigmoid(t)
+
+
+def _layer_default_gate_half(h, **kw):
+    out = _orig_layer(h, **kw)
+    if kw.get("shared_gate_bits") is not None:
+        return out
+    return _shared_gate_swapped(out, 0.5)
+
+
 MUTANTS = {
     "dropped bias": ("dequant", _dequant_no_bias),
     "swapped nibble order": ("unpack_codes", _unpack_swapped),
@@ -68,6 +98,9 @@ MUTANTS = {
     "silu sign": ("silu", _silu_neg),
     "router transposed": ("router_logits", _router_transposed),
     "ties to high index": ("topk", _topk_high_index_ties),
+    "silu on up": ("expert_forward", _expert_silu_on_up),
+    "shared gate sign": ("layer_decode", _layer_gate_sign),
+    "default shared gate 0.5": ("layer_decode", _layer_default_gate_half),
 }
 
 PINS = [getattr(P, n) for n in dir(P) if n.startswith("test_")]

@@ -303,3 +303,77 @@ def test_packed_bytes_tiny_and_two_bit():
     assert O.packed_expert_bytes(256, 128, 4) == 55_296
     assert O.packed_expert_bytes(4096, 1024, 2) == 3_932_160
     assert O.packed_expert_bytes(256, 128, 2) == 30_720
+
+
+# --------------------------------------------------------------------------- SwiGLU order and the shared gate
+def _unit_expert(H, I, gate_code, up_code):
+    """An expert whose gate and up rows all dequantise to the integer codes
+    given (scale 1, bias 0), so that g and u are known sums of x."""
+    one = np.full((I, H // 64), 0x3F80, np.uint16)
+    zero = np.zeros((I, H // 64), np.uint16)
+    ex = {"bits": 4, "group": 64}
+    ex["gate"] = (_const_matrix(I, H, gate_code, 0x3F80, 0)[0], one, zero)
+    ex["up"] = (_const_matrix(I, H, up_code, 0x3F80, 0)[0], one, zero)
+    ex["down"] = _const_matrix(H, I, 1, 0x3F80, 0)
+    return ex
+
+
+def test_swiglu_is_silu_of_gate_times_up():
+    """SwiGLU order ("397B MoE sur MacBook", "Techniques de rupture" item 4: the
+    fused SwiGLU): a = silu(g) * u, not silu(u) * g.  With x = e_0 the gate rows
+    give g = 1 and the up rows u = 2, so every a must be 2 * sigmoid(1) =
+    2e / (1 + e) = 1.4621..., while the swapped order would give
+    silu(2) = 2 / (1 + e^-2) = 1.7616...  Also: a is linear in u (doubling the
+    up codes doubles a exactly) but not in g."""
+    H, I = 64, 64
+    x = np.zeros(H)
+    x[0] = 1.0
+    out = O.expert_forward(_unit_expert(H, I, 1, 2), x, H, I)
+    assert np.all(out["g"] == 1.0) and np.all(out["u"] == 2.0)
+    assert np.allclose(out["a"], 2.0 * math.e / (1.0 + math.e), rtol=0, atol=1e-15)
+    assert not np.allclose(out["a"], 2.0 / (1.0 + math.exp(-2.0)), rtol=0, atol=1e-3)
+    # the down rows (all codes 1, scale 1) sum the 64 activations
+    assert np.allclose(out["d"], 64 * 2.0 * math.e / (1.0 + math.e), rtol=0, atol=1e-12)
+    a_u4 = O.expert_forward(_unit_expert(H, I, 1, 4), x, H, I)["a"]
+    a_g2 = O.expert_forward(_unit_expert(H, I, 2, 2), x, H, I)["a"]
+    assert np.allclose(a_u4, 2.0 * out["a"], rtol=0, atol=1e-15)
+    assert not np.allclose(a_g2, 2.0 * out["a"], rtol=0, atol=1e-3)
+
+
+def _gate_layer_case(shared_gate_bits):
+    """A tiny layer with h = 1 everywhere and eps = 0, so xn = 1 exactly, and a
+    shared expert whose output is known: gate codes 1, up codes 1 give g = u = H
+    per row, a = silu(H) * H; the down rows sum the activations."""
+    H, I, E = 128, 64, 8
+    ex, _, R = _tiny_layer(H=H, I=I, E=E)
+    sh = _unit_expert(H, I, 1, 1)
+    h = np.ones(H)
+    out = O.layer_decode(h, experts=ex, shared=sh, router_bits=R, top_k=4, hidden=H, inter=I, eps=0.0,
+                         shared_gate_bits=shared_gate_bits)
+    a = H / (1.0 + math.exp(-H)) * H
+    d_s = np.full(H, I * a)
+    routed = sum(out["w"][k] * O.expert_forward(ex[int(e)], np.ones(H), H, I)["d"] for k, e in enumerate(out["chosen"]))
+    return out, h, d_s, routed
+
+
+def test_shared_gate_is_sigmoid_of_gate_dot_xn():
+    """The "gate" of "MoE combine + residual + gate" ("Flash-MoE - Dizüstünde
+    ...", "Metal Compute Shaders"), read as g_s = sigmoid(shared_gate . xn).
+    With xn = 1 and a gate vector whose only nonzero entries are +2 and -0.5,
+    shared_gate . xn = 1.5 and g_s = 1 / (1 + e^-1.5) = 0.8175744762; the
+    opposite sign would give 0.1824255238.  y - h - (routed part) must be
+    g_s times the shared expert's output."""
+    g = np.zeros(128, np.uint16)
+    g[5] = 0x4000   # +2.0
+    g[77] = 0xBF00  # -0.5
+    out, h, d_s, routed = _gate_layer_case(g)
+    assert out["g_shared"] == pytest.approx(0.8175744761936437, abs=1e-15)
+    assert np.allclose(out["y"] - h - routed, 0.8175744761936437 * d_s, rtol=1e-13, atol=0)
+
+
+def test_shared_expert_default_gate_is_one():
+    """Without a shared-gate vector the shared expert is added as it is
+    (g_s = 1): y - h - (routed part) equals its output exactly."""
+    out, h, d_s, routed = _gate_layer_case(None)
+    assert out["g_shared"] == 1.0
+    assert np.allclose(out["y"] - h - routed, d_s, rtol=1e-13, atol=0)
