@@ -177,10 +177,14 @@ def moe_layer_decode(layer: N.moe_layer, h, ws, logit_offset=None, idx_out=None,
            "moe_layer_decode")
 
 
-def moe_layer_decode_noalloc(layer: N.moe_layer, h, logit_offset=None, idx_out=None, w_out=None, status_out=None,
+def moe_layer_decode_noalloc(layer: N.moe_layer, h, status_out, logit_offset=None, idx_out=None, w_out=None,
                              stream=None) -> None:
     """Single-token layer without a caller workspace (the library's fixed
-    device array instead; see include/moe.h).  h is [1, hidden]."""
+    device array instead; see include/moe.h).  h is [1, hidden]; status_out is
+    a device int32 that receives the call's device status (required: it is the
+    only record of a device-side error)."""
+    if status_out is None:
+        raise ValueError("moe_layer_decode_noalloc: status_out is required")
     B, (ph, po, pi, pw) = _layer_io(layer, h, logit_offset, idx_out, w_out)
     if B != 1:
         raise ValueError("moe_layer_decode_noalloc takes one token")

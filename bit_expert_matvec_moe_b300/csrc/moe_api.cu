@@ -11,9 +11,22 @@
 
 using namespace moe;
 
+// The tensor-core contraction (MOE_TENSOR_CORES) is accepted only when this is
+// 1; with 0 both entry points that take the flag refuse it with
+// MOE_ERR_UNSUPPORTED.
+#ifndef MOE_TC_ENABLED
+#define MOE_TC_ENABLED 0
+#endif
+
 namespace {
 
 thread_local std::string g_last_error;
+
+bool tc_refused(const moe_dims& d, int B) {
+  if (MOE_TC_ENABLED || B <= 1 || !(d.flags & MOE_TENSOR_CORES)) return false;
+  g_last_error = "MOE_TENSOR_CORES: the tensor-core contraction is not enabled in this build";
+  return true;
+}
 
 moe_status cuda_fail(cudaError_t e) {
   g_last_error = cudaGetErrorString(e);
@@ -278,11 +291,7 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int H = dims->hidden, I = dims->inter;
   WsHeader* hdr = at<WsHeader>(ws, 0);
-  if (B > 1 && (dims->flags & MOE_TENSOR_CORES)) {
-    // not enabled until validated on the GPU (as in moe_layer_decode)
-    set_last_error("MOE_TENSOR_CORES: the tensor-core contraction is not enabled in this build");
-    return MOE_ERR_UNSUPPORTED;
-  }
+  if (tc_refused(*dims, B)) return MOE_ERR_UNSUPPORTED;
   if (B > 1 && (dims->flags & MOE_TENSOR_CORES)) {
     // one expert for tokens 0 .. B-1: a single work item through the shared-expert maps
     const size_t blob_bytes = make_fmt(bits, H, I).total;
@@ -399,13 +408,8 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   WsHeader* hdr = at<WsHeader>(ws, 0);
   const int shared_bits = has_shared ? layer->shared_bits : d.bits;
   cudaError_t e;
-  // The tensor-core contraction is compiled and host-checked but has not run
-  // on a GPU yet: refused until it has been validated there.
+  if (tc_refused(d, B)) return MOE_ERR_UNSUPPORTED;
   const bool use_tc = B > 1 && (d.flags & MOE_TENSOR_CORES);
-  if (use_tc) {
-    set_last_error("MOE_TENSOR_CORES: the tensor-core contraction is not enabled in this build");
-    return MOE_ERR_UNSUPPORTED;
-  }
 
   if (B == 1 && !(d.flags & MOE_NO_FUSED)) {
     DecodePlan plan;

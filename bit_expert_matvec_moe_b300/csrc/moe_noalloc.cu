@@ -8,8 +8,8 @@
 //
 // The array is a file-scope static __device__ symbol; every GPU that loads the
 // library holds it until the process exits.  Host code cannot use the symbol's
-// name as a device address: the address is fetched with cudaGetSymbolAddress,
-// once per device, with that device current.
+// name as a device address: the address is fetched with cudaGetSymbolAddress
+// on each call, with the caller's device current.
 #include <mutex>
 #include <string>
 
@@ -34,25 +34,27 @@ moe_status fail(cudaError_t e, const char* what) {
   return MOE_ERR_CUDA;
 }
 
-// Device address of the scratch array on `dev` (current), set up on first use.
-moe_status scratch_for(int dev, void** out) {
+// Device address of the scratch array on `dev` (current).  The address is
+// looked up on every call (cheap), so that a module reloaded after a device
+// reset is noticed; whenever it differs from the one seen before on this
+// device, the whole array is cleared on `s` first (the launch counters and the
+// epoch words of published results must start together at zero).  The clear
+// is stream-ordered: it synchronises nothing else on the device.
+moe_status scratch_for(int dev, cudaStream_t s, void** out) {
   if (dev < 0 || dev >= kMaxDevices) {
     set_last_error("device index out of range");
     return MOE_ERR_UNSUPPORTED;
   }
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+  if (e != cudaSuccess) return fail(e, "cudaGetSymbolAddress");
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess) return fail(e, "cudaGetSymbolAddress");
-    // the launch counters and the epoch words must start together at zero
-    e = cudaMemset(p, 0, kScratchBytes);
-    if (e != cudaSuccess) return fail(e, "clearing the scratch array");
-    e = cudaDeviceSynchronize();
+  if (g_addr[dev] != p) {
+    e = cudaMemsetAsync(p, 0, kScratchBytes, s);
     if (e != cudaSuccess) return fail(e, "clearing the scratch array");
     g_addr[dev] = p;
   }
-  *out = g_addr[dev];
+  *out = p;
   return MOE_OK;
 }
 
@@ -81,7 +83,7 @@ moe_status moe_layer_decode_noalloc(const moe_layer* layer, float* h, const floa
   if (!a16(h) || !a16(layer->experts) || !a16(layer->router) || (has_shared && !a16(layer->shared)) ||
       (layer->rms_gamma && !a16(layer->rms_gamma)) || (has_gate && !a16(layer->shared_gate)) ||
       (logit_offset && !a16(logit_offset)) || (idx_out && !a16(idx_out)) || (w_out && !a16(w_out)) ||
-      (reinterpret_cast<uintptr_t>(status_out) & 3u))
+      !status_out || (reinterpret_cast<uintptr_t>(status_out) & 3u))
     return MOE_ERR_INVALID_ARG;
 
   // sizes: the scratch holds the header, E + 1 published logits and
@@ -103,11 +105,11 @@ moe_status moe_layer_decode_noalloc(const moe_layer* layer, float* h, const floa
     set_last_error("shape outside the single-token kernel (hidden <= 4096, inter <= 2048, shared memory plan)");
     return MOE_ERR_UNSUPPORTED;
   }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* scratch = nullptr;
-  moe_status st = scratch_for(dev, &scratch);
+  moe_status st = scratch_for(dev, s, &scratch);
   if (st != MOE_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(scratch);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // each call starts with a clear error state (the launch counters live on)
   e = cudaMemsetAsync(base, 0, kHeaderErrorBytes, s);
@@ -139,11 +141,10 @@ moe_status moe_layer_decode_noalloc(const moe_layer* layer, float* h, const floa
   f.plan = plan;
   e = launch_decode(f, (d.flags & MOE_PDL) != 0, s);
   if (e != cudaSuccess) return fail(e, "launch");
-  if (status_out) {
-    // the device status word of this call (0 = ok), copied on the stream
-    e = cudaMemcpyAsync(status_out, base, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
-    if (e != cudaSuccess) return fail(e, "cudaMemcpyAsync");
-  }
+  // the device status word of this call (0 = ok), copied on the stream: the
+  // caller cannot reach the array, and the next call clears it
+  e = cudaMemcpyAsync(status_out, base, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return fail(e, "cudaMemcpyAsync");
   return MOE_OK;
 }
 

@@ -222,15 +222,21 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream);
  * loads the library holds it until the process exits).  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *   layer, h, logit_offset, idx_out, w_out   as in moe_layer_decode, B = 1
- *   status_out   device int32 or NULL: receives this call's device status bits
- *                (0 ok; 1 a bounded wait ran out, as MOE_ERR_TIMEOUT; 2 a
- *                non-finite activation, as MOE_ERR_NONFINITE), copied on stream
+ *   status_out   device int32, required: receives this call's device status
+ *                bits (0 ok; 1 a bounded wait ran out, as MOE_ERR_TIMEOUT; 2 a
+ *                non-finite activation, as MOE_ERR_NONFINITE), copied on
+ *                stream.  The caller cannot read the array itself and the next
+ *                call clears the error state, so this copy is the only record
+ *                of a device-side error; NULL is refused (MOE_ERR_INVALID_ARG).
  * Returns MOE_ERR_UNSUPPORTED (text in moe_last_error_message) when the layer
  * needs more scratch than the array holds ((experts + 1) + (top_k + 1) * inter
  * eight-byte words plus a 256-byte header) or falls outside the single-token
  * kernel (hidden <= 4096, inter <= 2048).
- * The first call on a device looks up the array's address and clears it with a
- * synchronous cudaMemset, so make that first call before any stream capture.
+ * The array's device address is looked up on every call.  The first call on a
+ * device (and the first after a device reset reloads the library's module)
+ * also enqueues a clear of the whole array on `stream` before the kernel; it
+ * synchronises nothing else, but it is a memset node if captured, so make that
+ * first call before any stream capture.
  * Every call shares the one array and keeps its contents for the next call:
  * calls that may overlap on the GPU (different streams, or graphs replayed
  * concurrently) race and must be serialised by the caller.

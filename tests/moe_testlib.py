@@ -71,6 +71,15 @@ class DeviceLayer:
         return M.make_layer(self.dims, self.experts, self.stride, self.router, shared=self.shared,
                             shared_bits=self.shared_bits, rms_gamma=self.gamma, shared_gate=self.gate)
 
+    def oracle_many(self, h, offset=None, threads: int = 8) -> list:
+        """The oracle on every token of a batch (see oracle_batch)."""
+        d = self.dims
+        return oracle_batch(np.asarray(h, dtype=np.float64), experts=self.host_expert,
+                            shared=self.host_expert(G.SHARED_EXPERT) if self.shared is not None else None,
+                            router_bits=self.router_np, top_k=d.top_k, hidden=d.hidden, inter=d.inter,
+                            eps=d.rms_eps, gamma_bits=self.gamma_np, shared_gate_bits=self.gate_np,
+                            offset=offset, threads=threads)
+
     def oracle(self, h, offset=None, force_chosen=None) -> dict:
         d = self.dims
         return O.layer_decode(np.asarray(h, dtype=np.float64), experts=self.host_expert,
@@ -78,6 +87,62 @@ class DeviceLayer:
                               router_bits=self.router_np, top_k=d.top_k, hidden=d.hidden, inter=d.inter,
                               eps=d.rms_eps, gamma_bits=self.gamma_np, shared_gate_bits=self.gate_np,
                               offset=offset, force_chosen=force_chosen)
+
+
+def oracle_batch(h, *, experts, shared, router_bits, top_k, hidden, inter, eps=1e-6, gamma_bits=None,
+                 shared_gate_bits=None, offset=None, threads: int = 8) -> list:
+    """O.layer_decode on every row of h [B, H], composed from the oracle's own
+    functions so that each touched expert is dequantised once: the routing of
+    each token as in O.layer_decode, then O.expert_forward of each unique
+    expert on the matrix whose columns are its tokens' xn (a matrix product is
+    the matvec of each column), then the same combine.  Per token the result is
+    the oracle's (tests/test_oracle_batch.py checks it against O.layer_decode).
+    Experts are evaluated on a thread pool (numpy releases the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    get = experts if callable(experts) else (lambda e: experts[e])
+    h = np.asarray(h, dtype=np.float64)
+    B = h.shape[0]
+    toks = []
+    for b in range(B):
+        xn = O.rmsnorm(h[b], gamma_bits, eps)
+        logits = O.router_logits(router_bits, xn, None if offset is None else offset[b])
+        chosen = O.topk(logits, top_k)
+        toks.append({"xn": xn, "logits": logits, "chosen": chosen, "w": O.routing_weights(logits, chosen)})
+    users = {}
+    for b, t in enumerate(toks):
+        for k, e in enumerate(t["chosen"]):
+            users.setdefault(int(e), []).append((b, k))
+    XN = np.stack([t["xn"] for t in toks], axis=1)  # [H, B]
+
+    def run(item):
+        e, lst = item
+        cols = [b for b, _ in lst]
+        return e, O.expert_forward(get(e), XN[:, cols], hidden, inter)["d"]
+
+    with ThreadPoolExecutor(max_workers=max(1, threads)) as pool:
+        d_by_e = dict(pool.map(run, sorted(users.items())))
+        d_s = pool.submit(lambda: O.expert_forward(shared, XN, hidden, inter)["d"]).result() if shared is not None else None
+    out = []
+    for b, t in enumerate(toks):
+        d_routed = []
+        for k, e in enumerate(t["chosen"]):
+            col = [bb for bb, _ in users[int(e)]].index(b)
+            d_routed.append(d_by_e[int(e)][:, col])
+        y = h[b].copy()
+        for wk, dk in zip(t["w"], d_routed):
+            y = y + wk * dk
+        r = {**t, "d_routed": d_routed}
+        if shared is not None:
+            g_s = 1.0
+            if shared_gate_bits is not None:
+                g_s = 1.0 / (1.0 + np.exp(-(O.bf16_to_f64(shared_gate_bits) @ t["xn"])))
+            y = y + g_s * d_s[:, b]
+            r["d_shared"] = d_s[:, b]
+            r["g_shared"] = g_s
+        r["y"] = y
+        out.append(r)
+    return out
 
 
 def _to_dev(arr, torch, dtype=None):

@@ -59,8 +59,8 @@ def decode(L, h_np, offset=None, flags_extra=0, ws=None):
     return h.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
 
 
-def check_token(L, h_tok, y, idx, w, offset=None):
-    ref = L.oracle(h_tok, offset=offset)
+def check_token(L, h_tok, y, idx, w, offset=None, ref=None):
+    ref = L.oracle(h_tok, offset=offset) if ref is None else ref
     ok, tie = routing_ok(idx, ref["logits"], L.dims.top_k)
     assert ok, (idx, O.topk(ref["logits"], L.dims.top_k))
     if tie:
@@ -70,6 +70,14 @@ def check_token(L, h_tok, y, idx, w, offset=None):
     assert rel_err(y, ref["y"]) <= REL_TOL, rel_err(y, ref["y"])
     assert rel_err(y - h_tok, ref["y"] - h_tok) <= REL_TOL, rel_err(y - h_tok, ref["y"] - h_tok)
     return ref
+
+
+def check_batch(L, h, y, idx, w, offset=None):
+    """Every token of a batch against the oracle (each touched expert
+    dequantised once for all of its tokens)."""
+    refs = L.oracle_many(h, offset=offset)
+    for t in range(h.shape[0]):
+        check_token(L, h[t], y[t], idx[t], w[t], offset=None if offset is None else offset[t], ref=refs[t])
 
 
 # --------------------------------------------------------------------------- generator + packing
@@ -268,16 +276,16 @@ def test_fused_is_deterministic(full4):
     assert np.array_equal(y1, y2) and np.array_equal(i1, i2) and np.array_equal(w1, w2)
 
 
-def test_layer_batched_full_width_skewed(full4):
-    """Batched decode with per-expert popularity offsets: several tokens share
-    experts; each token must still equal its own oracle result."""
-    B = 8
+@pytest.mark.parametrize("B", [8, 32, 128])
+def test_layer_batched_full_width_skewed(full4, B):
+    """Batched decode with per-expert popularity offsets (the batched sweep's
+    routing): tokens share experts, and every token must equal its own oracle
+    result.  B = 32 and 128 split the shared expert into several work items."""
     h = G.hidden_states(G.SEED, 7, B, 4096)
     off = np.tile(G.popularity_offsets(G.SEED, 0, 512), (B, 1))
     y, idx, w = decode(full4, h, offset=off)
     assert len(np.unique(idx)) < B * 4  # experts are shared inside the batch
-    for t in (0, 5):
-        check_token(full4, h[t], y[t], idx[t], w[t], offset=off[t])
+    check_batch(full4, h, y, idx, w, offset=off)
 
 
 @pytest.mark.parametrize("B", [1, 8])
@@ -286,8 +294,7 @@ def test_layer_two_bit_full_width(B):
     L = build_layer(D(FULL, bits=2), gen="device")
     h = G.hidden_states(G.SEED, 9, B, 4096)
     y, idx, w = decode(L, h)
-    for t in sorted({0, B - 1}):
-        check_token(L, h[t], y[t], idx[t], w[t])
+    check_batch(L, h, y, idx, w)
 
 
 @pytest.mark.parametrize("path", ["fused", "fused_pdl", "multi"])
@@ -339,14 +346,13 @@ def test_layer_batch_edges():
     L = build_layer(D(TINY))
     h = G.hidden_states(G.SEED, 12, 33, 256)
     y, idx, w = decode(L, h)
-    for t in (0, 17, 32):
-        check_token(L, h[t], y[t], idx[t], w[t])
+    check_batch(L, h, y, idx, w)
     off = np.zeros((16, 16), np.float32)
     off[:, [3, 7, 9, 12]] = 30.0
     hs = G.hidden_states(G.SEED, 13, 16, 256)
     y, idx, w = decode(L, hs, offset=off)
     assert all(sorted(r) == [3, 7, 9, 12] for r in idx.tolist())
-    check_token(L, hs[4], y[4], idx[4], w[4], offset=off[4])
+    check_batch(L, hs, y, idx, w, offset=off)
 
 
 # --------------------------------------------------------------------------- device status

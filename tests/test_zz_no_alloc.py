@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from synth import generate as G
-from tests.moe_testlib import REL_TOL, build_layer, rel_err, workspace
+from tests.moe_testlib import REL_TOL, build_layer, rel_err, routing_ok, workspace
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -43,7 +43,7 @@ def _decode_noalloc(L, h_np):
     idx = torch.empty((1, L.dims.top_k), dtype=torch.int32, device="cuda")
     w = torch.empty((1, L.dims.top_k), dtype=torch.float32, device="cuda")
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
-    M.moe_layer_decode_noalloc(L.c_layer(), h, idx_out=idx, w_out=w, status_out=status)
+    M.moe_layer_decode_noalloc(L.c_layer(), h, status, idx_out=idx, w_out=w)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return h.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
@@ -61,6 +61,14 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(shape):
         assert rel_err(w, w_ref) <= REL_TOL
         assert rel_err(y[0], y_ref[0]) <= REL_TOL
         assert rel_err(y[0] - hs[t], y_ref[0] - hs[t]) <= REL_TOL
+        # and against the oracle itself, not only the other CUDA entry point
+        ref = L.oracle(hs[t])
+        ok, tie = routing_ok(idx[0], ref["logits"], L.dims.top_k)
+        assert ok
+        if tie:
+            ref = L.oracle(hs[t], force_chosen=idx[0])
+        assert rel_err(y[0], ref["y"]) <= REL_TOL
+        assert rel_err(y[0] - hs[t], ref["y"] - hs[t]) <= REL_TOL
 
 
 def test_noalloc_rejects_layers_beyond_its_array():
@@ -74,7 +82,25 @@ def test_noalloc_rejects_layers_beyond_its_array():
     router = torch.empty((1024, 4096), dtype=torch.int16, device="cuda")
     layer = M.make_layer(d, fake, stride, router, shared=fake)
     h = torch.zeros((1, 4096), dtype=torch.float32, device="cuda")
+    status = torch.zeros((1,), dtype=torch.int32, device="cuda")
     with pytest.raises(M.MoeError) as err:
-        M.moe_layer_decode_noalloc(layer, h)
+        M.moe_layer_decode_noalloc(layer, h, status)
     assert err.value.status == N.MOE_ERR_UNSUPPORTED
     assert "scratch array" in str(N.load().moe_last_error_message().decode())
+
+
+def test_noalloc_requires_a_status_word():
+    """The status copy is the only record of a device-side error (the array is
+    out of the caller's reach and the next call clears it), so the C entry
+    point refuses a NULL status pointer."""
+    from bit_expert_matvec_moe_b300 import _native as N
+
+    L = build_layer(M.Dims(flags=M.MOE_HAS_SHARED, hidden=256, inter=128, n_experts=16, top_k=4))
+    h = torch.from_numpy(G.hidden_states(G.SEED, 42, 1, 256)).cuda()
+    lib = N.load()
+    layer = L.c_layer()
+    import ctypes
+
+    st = lib.moe_layer_decode_noalloc(ctypes.byref(layer), h.data_ptr(), None, None, None, None,
+                                      torch.cuda.current_stream().cuda_stream)
+    assert st == N.MOE_ERR_INVALID_ARG
