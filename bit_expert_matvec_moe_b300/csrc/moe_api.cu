@@ -58,7 +58,8 @@ struct WsLayout {
 };
 
 // Byte offsets of the workspace regions for a batch of B tokens.  Only the
-// 256-byte header (status word, barrier counters) lives across calls.
+// 256-byte header (status word, launch and exchange counters) lives across
+// calls.
 WsLayout ws_layout(const moe_dims& d, int B) {
   WsLayout L{};
   size_t o = kHeaderBytes;
@@ -70,6 +71,10 @@ WsLayout ws_layout(const moe_dims& d, int B) {
   const size_t E = d.n_experts, K = d.top_k, H = d.hidden, I = d.inter;
   const size_t ns = K + 1;  // routed slots plus the shared slot
   const size_t ngh = H / MOE_GROUP, ngi = I / MOE_GROUP;
+  // the single-token kernel's published words first, at offsets that do not
+  // depend on the batch (epoch << 32 | value)
+  L.pub_logits = take((size_t)(MOE_MAX_EXPERTS + 1) * 8);
+  L.pub_act = take(ns * I * 8);
   L.logits = take(B * (E + 1) * 4);
   L.idx = take(B * K * 4);
   L.w = take(B * K * 4);
@@ -86,9 +91,6 @@ WsLayout ws_layout(const moe_dims& d, int B) {
   L.uniq_e = take((E + shared_items) * 4);
   L.uniq_off = take((E + shared_items + 1) * 4);
   L.ent = take(B * ns * 4);
-  // published words of the single-token kernel (epoch << 32 | value)
-  L.pub_logits = take((E + 1) * 8);
-  L.pub_act = take(ns * I * 8);
   if (d.flags & MOE_TENSOR_CORES) {
     const size_t ne = B * ns;  // entries: (token, slot) pairs
     L.xops = take(ne * 2 * H * 2);

@@ -45,6 +45,15 @@ namespace {
 
 __device__ __forceinline__ int lo_row(int c, int P, int n) { return (int)((long long)c * n / P); }
 
+// Phase stamps (globaltimer) of every block, in builds with MOE_TIMELINE only.
+#ifdef MOE_TIMELINE
+constexpr int kStamps = 32;
+__device__ unsigned long long g_timeline[1024 * kStamps];
+#define STAMP(i) (g_timeline[blockIdx.x * kStamps + (i)] = globaltimer())
+#else
+#define STAMP(i) ((void)0)
+#endif
+
 // Slot of activation value i in its expert's published vector: inside each
 // group of 64, value 4j + t goes to slot 16t + j, so that the half-warp that
 // reads a group (lane j takes values 4j .. 4j+3) reads 16 consecutive words per
@@ -208,6 +217,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   // Barrier set-up, visible to every thread and to the copy engine before the
   // first copy is issued:
   if (tid == 0) {
+    STAMP(0);
     for (int i = 0; i < nbar; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
     fence_proxy_async();
@@ -275,6 +285,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   }
   if (__syncthreads_or(tid == 0 && *(volatile uint32_t*)&a.hdr->abort)) goto cleanup;
   warp_wait(bar_h);
+  if (tid == 0) STAMP(1);
   {
     float4 hv0 = 4 * tid < H ? reinterpret_cast<const float4*>(hbuf)[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 hv1 =
@@ -316,6 +327,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     ss = warp_sum(ss);
     if (lane == 0) s_red[wid] = ss;
     const int nonfinite_x = __syncthreads_or(!finite);
+    if (tid == 0) STAMP(2);
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) tot += s_red[w];
@@ -361,6 +373,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
 
     // ---- router rows -> published logits (each thread's 8 values of x against each row)
     if (nrr > 0) warp_wait(0);
+    if (tid == 0) STAMP(3);
     {
       const uint8_t* rt = G + a.plan.off_rt;
       for (int ri = 0; ri < nrr; ++ri) {
@@ -397,6 +410,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       __syncwarp();
       if (lane == 0) {
         red_relaxed_add_u64(&a.hdr->published_logits, 1ull);
+        STAMP(4);
         s_mask[4] |= 1u;
       }
     }
@@ -417,8 +431,10 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       if (wid != 0) named_arrive(1, kBlock);
       if (wid == 0) {
         named_sync(1, kBlock);
+        if (lane == 0) STAMP(5);
         bool ok = true;
         bool ready = lane != 0 || wait_count(a.hdr, &a.hdr->published_logits, (unsigned long long)P * expect);
+        if (lane == 0) STAMP(6);
         ready = __all_sync(0xffffffffu, ready);
         uint32_t key[32];
 #pragma unroll
@@ -474,6 +490,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
               }
             }
             s_mask[0] = issued;
+            STAMP(7);
             chosen_softmax(s_val, K, s_coef + hs);
             if (hs) s_coef[0] = a.has_gate ? 1.0f / (1.0f + expf(-gate_logit)) : 1.0f;
             if (c == 0) {
@@ -497,6 +514,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       load_x(xl, xe);
       for (int k = 0; k < K; ++k) {
         gate_up(hs + k, G + (size_t)k * gu_slot, a.bits, xl, xe);
+        if (tid == 0) STAMP(8 + k);
         // routed down rows are needed last: warp 0 issues expert k's copy once
         // its gate/up rows have landed (warp 0 has gate/up rows whenever the
         // block has any, and gate_up waited for them), which keeps the copies
@@ -516,6 +534,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     // ---- SwiGLU of every expert's rows, weighted by the expert's routing
     // coefficient, published for every block
     if (failed()) goto cleanup;
+    if (tid == 0) STAMP(16);
     for (int t = tid; t < NE * nr; t += kBlock) {
       const int p = t / nr, i = t - p * nr;
       const float* pb = part + (size_t)p * part_stride;
@@ -536,7 +555,9 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     // are complete: block barrier above), then every thread checks the epochs
     // of the words it needs and polls a late word again
     if (tid == 0) {
+      STAMP(17);
       const bool ok = wait_count(a.hdr, &a.hdr->published_act, (unsigned long long)P * expect);
+      STAMP(18);
       if (ok) {
         fence_proxy_async();
         mbar_expect_tx(&bar[bar_a], (uint32_t)a.plan.abuf_bytes);
@@ -547,6 +568,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     }
     if (__syncthreads_or(tid == 0 && s_mask[5] != 0u)) goto cleanup;
     warp_wait(bar_a);
+    if (tid == 0) STAMP(19);
 
     // ---- limbs of every weighted a: a half-warp per group, 2 groups per warp
     // per pass, kActPasses passes quantised together
@@ -590,6 +612,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       if (__syncthreads_or(!fin) && tid == 0) atomicOr(&a.hdr->status, ST_NONFINITE);
     }
     if (failed()) goto cleanup;
+    if (tid == 0) STAMP(20);
 
     // ---- down rows of every expert as one long dot product per row: thread
     // (set, q) takes unit q = (expert p, group g) of rows set, set + S, ...;
@@ -623,6 +646,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         }
       }
       if (failed()) goto cleanup;
+      if (tid == 0) STAMP(21);
       // row r: 16 threads sum every 16th partial, then a butterfly over the 16
       {
         const int r = tid >> 4, sub = tid & 15;
@@ -635,6 +659,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       }
       __syncthreads();
       if (tid < nj) a.h[j0 + tid] = hres + ysm[tid];
+      if (tid == 0) STAMP(22);
     }
   }
   return;
@@ -652,6 +677,12 @@ cleanup:
   }
   __syncthreads();
 }
+
+#ifdef MOE_TIMELINE
+extern "C" int moe_timeline_read(unsigned long long* host, int n) {
+  return (int)cudaMemcpyFromSymbol(host, g_timeline, sizeof(unsigned long long) * (size_t)n);
+}
+#endif
 
 bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, int shared_bits, int has_shared,
                      int has_gate, DecodePlan* out) {
