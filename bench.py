@@ -319,7 +319,8 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": (f"u{bits} codes dequantised to fp16 x fp16 hi/lo activations (tcgen05 kind::f16, fp32 accumulate)"
-                  if tc else f"u{bits} codes x fp32 activations (int32 dp4a group sums, fp32 accumulate)"),
+                  if tc else f"u{bits} codes x 23-bit block-floating-point activations (3 byte limbs per 64-group, "
+                             "exact int32 dp4a group sums), fp32 scale/bias and accumulation"),
         "data": "synthetic (seeded SplitMix64; random-init weights of the stated shape)",
         "config": {
             "workload": (f"full-width single MoE layer, batch {B}: hidden 4096, {d.n_experts} experts, top-4 routed + 1 shared, "
@@ -355,7 +356,7 @@ def run_ours(args, rank, world, local):
         # the oracle decodes token by token: batching does not change its tokens/s
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, bits=bits)
         ncpu = os.cpu_count() or 1
-        if ncpu > 1 and args.config == 2 and B == 1:  # the same oracle with its BLAS on every host core
+        if ncpu > 1 and args.config == 2 and B == 1:  # the same oracle with its rows split over every host core
             mt = cpu_baseline(args.cpu_seconds / 2, threads=ncpu)
             out["cpu_baseline"]["all_cores"] = {"value": mt["value"], "cores": mt["cores"], "sample": mt["sample"]}
     if rank == 0:
@@ -479,7 +480,8 @@ def run_stack(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "u4 codes x fp32 activations (int32 dp4a group sums, fp32 accumulate)",
+        "dtype": ("u4 codes x 23-bit block-floating-point activations (3 byte limbs per 64-group, exact int32 dp4a "
+                  "group sums), fp32 scale/bias and accumulation"),
         "data": "synthetic (seeded SplitMix64; random-init weights of the stated shape)",
         "config": {
             "workload": (f"{Lyr}-layer MoE decode stack resident in HBM: full-width 4-bit layers (hidden 4096, {E} experts, "
@@ -516,21 +518,46 @@ def run_stack(args, rank, world, local):
 # ----------------------------------------------------------------------------- oracle (CPU) timing
 def cpu_baseline(seconds: float, tokens_max: int = 64, threads: int = 1, bits: int = 4):
     """The fp64 oracle as it stands on a bounded sample of the same workload,
-    run in a child process whose BLAS uses `threads` threads (1: one core; the
-    oracle's matvecs are the only multi-threaded part)."""
-    t = str(threads)
-    env = dict(os.environ, OMP_NUM_THREADS=t, OPENBLAS_NUM_THREADS=t, MKL_NUM_THREADS=t, CUDA_VISIBLE_DEVICES="")
+    run in a child process on `threads` host threads (1: one core; more: the
+    rows of every matvec split over a thread pool, each BLAS call on one
+    thread)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
     res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", str(seconds),
-                          str(tokens_max), t, str(bits)], capture_output=True, text=True, env=env, timeout=600)
+                          str(tokens_max), str(threads), str(bits)], capture_output=True, text=True, env=env,
+                         timeout=600)
     if res.returncode != 0:
         raise RuntimeError("oracle timing failed: " + res.stderr[-2000:])
     return json.loads(res.stdout.strip().splitlines()[-1])
 
 
+def _expert_forward_rows(O, ex, xn, H, I, pool, threads):
+    """O.expert_forward with the rows of each matvec split over `threads`
+    threads: the oracle's own dequant and SiLU on row blocks (every row of a
+    matvec is independent, so the result is the oracle's)."""
+    bits, group = ex["bits"], ex["group"]
+
+    def rows(m, n_cols, x, lo, hi):
+        c, sc, bi = ex[m]
+        return O.dequant(c[lo:hi], sc[lo:hi], bi[lo:hi], bits, group, n_cols) @ x
+
+    def split(n):
+        step = (n + threads - 1) // threads
+        return [(i, min(n, i + step)) for i in range(0, n, step)]
+
+    g = np.concatenate(list(pool.map(lambda r: rows("gate", H, xn, *r), split(I))))
+    u = np.concatenate(list(pool.map(lambda r: rows("up", H, xn, *r), split(I))))
+    a = O.silu(g) * u
+    return np.concatenate(list(pool.map(lambda r: rows("down", I, a, *r), split(H))))
+
+
 def _cpu_baseline_child(seconds: float, tokens_max: int, threads: int = 1, bits: int = 4):
     """Tokens are decoded one by one until `seconds` of oracle time pass.  The
     touched experts are generated before each token's timing (input generation
-    is not oracle work)."""
+    is not oracle work).  With one thread this is O.layer_decode as it stands;
+    with several, the same layer with the rows of every matvec split over a
+    thread pool (numpy releases the interpreter lock in its kernels)."""
+    from concurrent.futures import ThreadPoolExecutor
+
     from oracle import moe_oracle as O
     from synth import generate as G
 
@@ -545,18 +572,35 @@ def _cpu_baseline_child(seconds: float, tokens_max: int, threads: int = 1, bits:
             cache[e] = G.expert(G.SEED, 0, e, H, I, bits)
         return cache[e]
 
+    pool = ThreadPoolExecutor(max_workers=threads) if threads > 1 else None
+
+    def decode(hh):
+        if pool is None:
+            return O.layer_decode(hh, experts=get, shared=shared, router_bits=R, top_k=K, hidden=H, inter=I)["y"]
+        xn = O.rmsnorm(hh, None, 1e-6)
+        logits = O.router_logits(R, xn)
+        chosen = O.topk(logits, K)
+        w = O.routing_weights(logits, chosen)
+        y = np.asarray(hh, dtype=np.float64).copy()
+        for wk, e in zip(w, chosen):
+            y = y + wk * _expert_forward_rows(O, get(int(e)), xn, H, I, pool, threads)
+        return y + _expert_forward_rows(O, shared, xn, H, I, pool, threads)
+
     done, spent = 0, 0.0
     while done < tokens_max and spent < seconds:
         xn = O.rmsnorm(h[done], None, 1e-6)
         for e in O.topk(O.router_logits(R, xn), K):
             get(int(e))  # generation outside the timed region
         t0 = time.perf_counter()
-        O.layer_decode(h[done], experts=get, shared=shared, router_bits=R, top_k=K, hidden=H, inter=I)
+        decode(h[done])
         spent += time.perf_counter() - t0
         done += 1
+    if pool is not None:
+        pool.shutdown()
+    how = ("fp64 numpy, 1 thread" if threads == 1 else
+           f"fp64 numpy, rows of every matvec split over {threads} threads")
     return {"value": round(done / spent, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{done} of the {TOKENS} decode tokens of the same layer ({bits}-bit routed experts), fp64 numpy, "
-                      f"{threads} BLAS thread{'s' if threads > 1 else ''}"}
+            "sample": f"{done} of the {TOKENS} decode tokens of the same layer ({bits}-bit routed experts), {how}"}
 
 
 def run_reference(args, rank, world):
