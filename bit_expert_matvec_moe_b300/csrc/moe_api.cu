@@ -11,11 +11,11 @@
 
 using namespace moe;
 
-// The tensor-core contraction (MOE_TENSOR_CORES) is accepted only when this is
-// 1; with 0 both entry points that take the flag refuse it with
-// MOE_ERR_UNSUPPORTED.
+// The tensor-core contraction (MOE_TENSOR_CORES) is accepted when this is 1
+// (the default); a build with 0 refuses the flag in both entry points that
+// take it, with MOE_ERR_UNSUPPORTED.
 #ifndef MOE_TC_ENABLED
-#define MOE_TC_ENABLED 0
+#define MOE_TC_ENABLED 1
 #endif
 
 namespace {
@@ -153,12 +153,6 @@ moe_status run_tc(const moe_dims& d, const WsLayout& L, void* ws, int B, int nsl
   tl.a_out = at<float>(ws, L.a);
   tl.d_out = at<float>(ws, L.d);
   tl.hdr = hdr;
-  // variant with the A operand in tensor memory: MOE_TC_A_IN_TMEM=1 in the environment
-  static const bool a_in_tmem = [] {
-    const char* v = std::getenv("MOE_TC_A_IN_TMEM");
-    return v && v[0] == '1';
-  }();
-  tl.a_in_tmem = a_in_tmem ? 1 : 0;
   if (!tc::tc_supported(tl)) {
     set_last_error("MOE_TENSOR_CORES: layer layout not supported by the tensor-core contraction");
     return MOE_ERR_UNSUPPORTED;

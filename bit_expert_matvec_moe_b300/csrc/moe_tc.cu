@@ -15,10 +15,12 @@
 //   warp 0     TMA producer: per unit, the code pieces and (scale, bias) words
 //              of 8 groups x 128 rows per stage (3 stages in flight);
 //   warp 1     TMA producer: per K-block (64 inputs) the entry rows of B;
-//   warp 2     owns the tensor memory (2 accumulators of 64 columns) and
-//              issues 4 MMAs (M 128, N 2 x tokens, K 16) per K-block;
-//   warps 3-6  epilogue: read an accumulator (one warp per lane quarter),
-//              add hi and lo columns, scale, SwiGLU for gate/up, store;
+//   warp 2     owns the tensor memory (a ring of 4 accumulators of 64
+//              columns) and issues 4 MMAs (M 128, N 2 x tokens, K 16) per
+//              K-block, starting a fresh accumulator every kSpanKB K-blocks;
+//   warps 3-6  epilogue: add up a unit's partial sums in fp32 registers
+//              (one warp per tensor-memory lane quarter), then add hi and lo
+//              columns, scale, SwiGLU for gate/up, store;
 //   warps 7-14 dequantise the staged codes into the A operand (fp16
 //              q*s + b, 128-byte swizzled) of 4 K-blocks in flight.
 // Every wait is bounded (1 s); a CTA that gives up records ST_TIMEOUT, lets
@@ -200,10 +202,6 @@ __device__ __forceinline__ void drain_ring(uint64_t* ring, int slots, uint32_t i
   for (uint32_t k = issued - n; k < issued; ++k) mbar_wait(&ring[k % slots], (k / slots) & 1u);
 }
 
-// kTmemA: the dequantised A operand goes to tensor memory (tcgen05.st, one
-// 32-column block per K slot after the accumulators) and the MMAs read it from
-// there, instead of a 128-byte-swizzled shared-memory tile.
-template <bool kTmemA>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_contract_kernel(const __grid_constant__ CUtensorMap m_codes, const __grid_constant__ CUtensorMap m_sb,
                        const __grid_constant__ CUtensorMap m_codes_sh, const __grid_constant__ CUtensorMap m_sb_sh,
@@ -216,8 +214,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* full_a = empty_c + kCodeSlots;   // A K-block written by the 8 dequantising warps
   uint64_t* full_b = full_a + kKSlots;       // B K-block landed (TMA bytes)
   uint64_t* empty_k = full_b + kKSlots;      // K-block read by the MMAs (commit)
-  uint64_t* dfull = empty_k + kKSlots;       // accumulator complete (commit)
-  uint64_t* dempty = dfull + kDBufs;         // accumulator read by the 4 epilogue warps
+  uint64_t* dfull = empty_k + kKSlots;       // partial sum complete (commit)
+  uint64_t* dempty = dfull + kDBufs;         // partial sum read by the 4 epilogue warps
   uint64_t* drain = dempty + kDBufs;
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kOffMisc);  // [0] tensor memory, [1] abort, [2] status bits
   volatile uint32_t* abort = misc + 1;
@@ -249,7 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tmap(&m_sb_sh);
     prefetch_tmap(&m_b);
   }
-  constexpr uint32_t kCols = kTmemA ? kTmemColsTs : kTmemCols;
+  constexpr uint32_t kCols = kTmemCols;
   if (warp == kWarpMma) {
     tmem_alloc(&misc[0], kCols);
     tmem_relinquish();
@@ -312,33 +310,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ---- MMAs ---------------------------------------------------------------
+    // Partial sums: a fresh accumulator (ring slot pc % kDBufs) every kSpanKB
+    // K-blocks of a unit, committed to dfull for the epilogue.
     if (lane == 0) {
-      uint32_t kc = 0, uc = 0;
+      uint32_t kc = 0, pc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const TcChunk ch = a.chunks[u / a.tiles];
         const uint32_t idesc = make_idesc_f16(kTcM, 2 * ((ch.n + 7) & ~7));
-        const uint32_t d = uc & 1u;
-        if (!(ok = tc_wait(&dempty[d], ((uc >> 1) & 1u) ^ 1u, abort))) break;
-        tc_fence_after();
-        const uint32_t dt = tmem + d * kDCols;
-        for (int kb = 0; kb < a.ng; ++kb, ++kc) {
-          const uint32_t slot = kc % kKSlots, par = (kc / kKSlots) & 1u;
-          if (!(ok = tc_wait(&full_a[slot], par, abort) && tc_wait(&full_b[slot], par, abort))) break;
+        for (int kb0 = 0; kb0 < a.ng && ok; kb0 += kSpanKB, ++pc) {
+          const uint32_t d = pc % kDBufs;
+          if (!(ok = tc_wait(&dempty[d], ((pc / kDBufs) & 1u) ^ 1u, abort))) break;
           tc_fence_after();
-          const uint32_t aa = su32(sm + kOffK + slot * kKSlotBytes), ba = aa + kABytes;
+          const uint32_t dt = tmem + d * kDCols;
+          const int kb1 = min(a.ng, kb0 + kSpanKB);
+          for (int kb = kb0; kb < kb1; ++kb, ++kc) {
+            const uint32_t slot = kc % kKSlots, par = (kc / kKSlots) & 1u;
+            if (!(ok = tc_wait(&full_a[slot], par, abort) && tc_wait(&full_b[slot], par, abort))) break;
+            tc_fence_after();
+            const uint32_t aa = su32(sm + kOffK + slot * kKSlotBytes), ba = aa + kABytes;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            if constexpr (kTmemA)
-              mma_f16_ts(dt, tmem + kTmemACol0 + slot * 32 + 8 * kk, sdesc_sw128_kmajor(ba + 32 * kk), idesc,
-                         (kb | kk) != 0);
-            else
+            for (int kk = 0; kk < 4; ++kk)
               mma_f16_ss(dt, sdesc_sw128_kmajor(aa + 32 * kk), sdesc_sw128_kmajor(ba + 32 * kk), idesc,
-                         (kb | kk) != 0);
+                         (kb != kb0 || kk != 0) ? 1u : 0u);
+            mma_commit(&empty_k[slot]);
           }
-          mma_commit(&empty_k[slot]);
+          if (ok) mma_commit(&dfull[d]);
         }
-        if (ok) mma_commit(&dfull[d]);
       }
       // every MMA issued by this CTA has finished reading shared memory
       mma_commit(drain);
@@ -346,45 +344,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (warp < kWarpDeq0) {
-    // ---- epilogue: accumulator -> outputs ------------------------------------
+    // ---- epilogue: partial sums -> outputs ------------------------------------
     const int q = warp & 3;
-    uint32_t uc = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
+    uint32_t pc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const TcChunk ch = a.chunks[u / a.tiles];
       const int row = (u % a.tiles) * kTcM + 32 * q + lane;
-      const uint32_t d = uc & 1u;
-      if (!tc_wait_warp(&dfull[d], (uc >> 1) & 1u, abort)) break;
-      tc_fence_after();
       const int n8 = (ch.n + 7) & ~7;
-      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + d * kDCols;
-      uint32_t v[4][16];
+      // this lane's row: token t's hi + lo sum, added up over the unit's partials
+      float acc[kTcTok];
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb)
-        if (8 * cb < n8) tmem_ld16(ta + 16 * cb, v[cb]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&dempty[d]);
+      for (int t = 0; t < kTcTok; ++t) acc[t] = 0.f;
+      for (int kb0 = 0; kb0 < a.ng; kb0 += kSpanKB, ++pc) {
+        const uint32_t d = pc % kDBufs;
+        if (!(ok = tc_wait_warp(&dfull[d], (pc / kDBufs) & 1u, abort))) break;
+        tc_fence_after();
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + d * kDCols;
+        uint32_t v[4][16];
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; cb < 4; ++cb)
+          if (8 * cb < n8) tmem_ld16(ta + 16 * cb, v[cb]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[d]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int t = 8 * cb + i;
-          if (t < ch.n) {
-            const int j = ch.e0 + t;
-            const int id = (j >= 0 && j < a.max_entries) ? a.ent[j] : -1;
-            if (id < 0 || id >= a.n_ids) {  // cannot happen with a consistent work list
-              if (lane == 0) atomicOr(&misc[2], ST_BOUNDS);
-              continue;
-            }
-            const float val = (__uint_as_float(v[cb][2 * i]) + __uint_as_float(v[cb][2 * i + 1])) * a.bscale[j];
-            const size_t o = (size_t)id * a.out_cols;
-            if (a.mode == 0) {
-              const float up = __shfl_xor_sync(0xffffffffu, val, 1);  // rows 2p (gate) and 2p + 1 (up)
-              if (!(lane & 1) && row < a.rows) a.out[o + (row >> 1)] = silu_mul(val, up);
-            } else if (row < a.rows) {
-              a.out[o + row] = val;
-            }
+        for (int cb = 0; cb < 4; ++cb)
+          if (8 * cb < n8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[8 * cb + i] += __uint_as_float(v[cb][2 * i]) + __uint_as_float(v[cb][2 * i + 1]);
+          }
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int t = 0; t < kTcTok; ++t) {
+        if (t < ch.n) {
+          const int j = ch.e0 + t;
+          const int id = (j >= 0 && j < a.max_entries) ? a.ent[j] : -1;
+          if (id < 0 || id >= a.n_ids) {  // cannot happen with a consistent work list
+            if (lane == 0) atomicOr(&misc[2], ST_BOUNDS);
+            continue;
+          }
+          const float val = acc[t] * a.bscale[j];
+          const size_t o = (size_t)id * a.out_cols;
+          if (a.mode == 0) {
+            const float up = __shfl_xor_sync(0xffffffffu, val, 1);  // rows 2p (gate) and 2p + 1 (up)
+            if (!(lane & 1) && row < a.rows) a.out[o + (row >> 1)] = silu_mul(val, up);
+          } else if (row < a.rows) {
+            a.out[o + row] = val;
           }
         }
       }
@@ -426,22 +434,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             dequant_word2(c.x, s2, b2, c0, c1);
             dequant_word2(c.y, s2, b2, c2, c3);
           }
-          if constexpr (kTmemA) {
-            // lane r of the tile, 16 columns = this half's 32 inputs
-            const uint32_t v[16] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w,
-                                    c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w};
-            tc_fence_after();  // the MMAs that read this slot have completed (empty_k)
-            tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + kTmemACol0 + ks * 32 + 16 * h, v);
-            tmem_st_wait();
-            tc_fence_before();
-          } else {
-            uint8_t* A = sm + kOffK + ks * kKSlotBytes;
-            *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 0)) = c0;
-            *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 1)) = c1;
-            *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 2)) = c2;
-            *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 3)) = c3;
-            fence_proxy_async();  // generic-proxy writes -> visible to the MMA (async proxy)
-          }
+          uint8_t* A = sm + kOffK + ks * kKSlotBytes;
+          *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 0)) = c0;
+          *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 1)) = c1;
+          *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 2)) = c2;
+          *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 3)) = c3;
+          fence_proxy_async();  // generic-proxy writes -> visible to the MMA (async proxy)
           __syncwarp();
           if (lane == 0) mbar_arrive(&full_a[ks]);
           ++kc;
@@ -573,9 +571,7 @@ cudaError_t launch_tc_contract(const TcLaunch& L, int mode, cudaStream_t s) {
   a.max_entries = L.max_entries;
   a.n_ids = L.max_entries;
   a.hdr = L.hdr;
-  static std::atomic<int> configured_ts[kMaxDevices];
-  cudaError_t e = L.a_in_tmem ? ensure_dynamic_smem(tc_contract_kernel<true>, (int)kSmemBytes, configured_ts)
-                              : ensure_dynamic_smem(tc_contract_kernel<false>, (int)kSmemBytes, configured);
+  cudaError_t e = ensure_dynamic_smem(tc_contract_kernel, (int)kSmemBytes, configured);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -583,10 +579,7 @@ cudaError_t launch_tc_contract(const TcLaunch& L, int mode, cudaStream_t s) {
   const long long max_units = (long long)L.max_chunks * a.tiles;
   const int grid = (int)(max_units < sms ? max_units : sms);
   if (grid <= 0) return cudaSuccess;
-  if (L.a_in_tmem)
-    tc_contract_kernel<true><<<grid, kTcThreads, kSmemBytes, s>>>(mc, ms, mcs, mss, mb, a);
-  else
-    tc_contract_kernel<false><<<grid, kTcThreads, kSmemBytes, s>>>(mc, ms, mcs, mss, mb, a);
+  tc_contract_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(mc, ms, mcs, mss, mb, a);
   return cudaGetLastError();
 }
 

@@ -58,11 +58,11 @@ typedef enum {
 #define MOE_PDL 8             /* moe_layer_decode, B == 1: programmatic dependent launch, so that the
                                  kernel's weight prefetch overlaps the previous kernel on the stream
                                  (instead of a cooperative launch; see moe_layer_decode) */
-#define MOE_TENSOR_CORES 16   /* moe_layer_decode, B > 1: expert matvecs as tensor-core contractions
-                                 (tcgen05, fp16 dequantised weights x fp16 hi/lo activations);
-                                 reserved: this build refuses it with MOE_ERR_UNSUPPORTED until the
-                                 kernels have been validated on the GPU.  Workspace sizes include the
-                                 path's operand buffers when the flag is set. */
+#define MOE_TENSOR_CORES 16   /* moe_layer_decode and moe_expert_forward, B > 1: expert matvecs as
+                                 tensor-core contractions (tcgen05, fp16 dequantised weights x fp16
+                                 hi/lo activations, partial sums of 256 inputs added in fp32).
+                                 Workspace sizes include the path's operand buffers when the flag
+                                 is set; moe_workspace_bytes must be given the same flags. */
 
 /* Limits of this implementation (checked on entry). */
 #define MOE_MAX_TOPK 8

@@ -99,11 +99,11 @@ def test_host_validation_returns_before_launch(lib):
     assert lib.moe_workspace_init(None, 0, None) == N.MOE_ERR_INVALID_ARG
 
 
-def test_tensor_core_flag_reserved(lib):
+def test_tensor_core_flag_workspace(lib):
     """MOE_TENSOR_CORES is a valid flag: the workspace grows by the tensor-core
     path's operand buffers (B rows of xn and of the activations, fp16 hi and lo,
-    per (token, slot) entry), and moe_layer_decode refuses it on the host for
-    B > 1 while the path is not enabled."""
+    per (token, slot) entry), and a call without its buffers is refused on the
+    host before anything is enqueued."""
     from bit_expert_matvec_moe_b300 import _native as N
 
     d = dims()
@@ -115,10 +115,9 @@ def test_tensor_core_flag_reserved(lib):
         assert w1 - w0 >= entries * 2 * (4096 + 1024) * 2
     layer = N.moe_layer(t, 16, 7_077_888, 32, 4, 48, None, None)
     ws = lib.moe_workspace_bytes(ctypes.byref(t), 8)
-    assert lib.moe_layer_decode(ctypes.byref(layer), 16, 8, None, None, None, 64, ws, None) == N.MOE_ERR_UNSUPPORTED
-    assert b"MOE_TENSOR_CORES" in lib.moe_last_error_message()
-    # moe_expert_forward refuses it the same way for B > 1
-    assert lib.moe_expert_forward(ctypes.byref(t), 4, 16, 32, 3, None, 48, 0, 64, ws, None) == N.MOE_ERR_UNSUPPORTED
+    assert lib.moe_layer_decode(ctypes.byref(layer), None, 8, None, None, None, 64, ws, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_decode(ctypes.byref(layer), 16, 8, None, None, None, None, ws, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_forward(ctypes.byref(t), 4, None, 32, 3, None, 48, 0, 64, ws, None) == N.MOE_ERR_INVALID_ARG
 
 
 def test_status_strings(lib):

@@ -1,14 +1,10 @@
 """Parity of the batched tensor-core contraction (MOE_TENSOR_CORES) with the
-fp64 oracle, through moe_layer_decode.
-
-Not collected by pytest under this name: the library still refuses the flag
-(the kernels have not run on a GPU yet).  Once moe_layer_decode accepts it,
-this file becomes tests/test_gpu_tensor_cores.py.  The first cases run
-one expert through moe_expert_forward (tiny shape first: a few KB, every
-kernel of the path once), then the tiny layer at B = 2; the later cases cover chunks
-of more than kTcTok = 32 entries, a ragged last code stage and row tile,
-2-bit routed experts, the full-width layer with skewed routing, and equality
-of the routing with the dp4a path."""
+fp64 oracle, through moe_expert_forward and moe_layer_decode: one expert on
+three tokens (tiny, odd and full-width shapes, 4- and 2-bit), the tiny layer
+at B = 2, chunks of more than kTcTok = 32 entries, a ragged last code stage
+and row tile, no shared expert, gamma and shared gate, 2-bit routed experts,
+the full-width layer with skewed routing (every token of B = 8 and 64, and
+equality of the routing with the dp4a path)."""
 import numpy as np
 import pytest
 
@@ -58,8 +54,8 @@ def decode_tc(L, h_np, offset=None, tc=True):
     return h.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
 
 
-def check(L, h_tok, y, idx, w, offset=None):
-    ref = L.oracle(h_tok, offset=offset)
+def check(L, h_tok, y, idx, w, offset=None, ref=None):
+    ref = L.oracle(h_tok, offset=offset) if ref is None else ref
     ok, tie = routing_ok(idx, ref["logits"], L.dims.top_k)
     assert ok
     if tie:
@@ -147,28 +143,15 @@ def test_tc_full_width_skewed(B):
     y2, idx2, w2 = decode_tc(L, h, offset=off, tc=False)
     assert (idx == idx2).all()  # routing does not depend on the contraction
     assert rel_err(y, y2) <= REL_TOL
-    for t in sorted({0, B // 2, B - 1}):
-        check(L, h[t], y[t], idx[t], w[t], offset=off[t])
-
-
-def test_tc_a_in_tensor_memory_variant():
-    """The A-in-tensor-memory variant (MOE_TC_A_IN_TMEM=1, read once per
-    process) on the tiny and the full-width layer, in a child process."""
-    import os
-    import subprocess
-    import sys
-
-    code = ("import tests.pending_gpu_tensor_cores as T; T.test_tc_tiny_two_tokens(); "
-            "T.test_tc_tiny_many_tokens_per_expert(4); T.test_tc_full_width_skewed(8)")
-    env = dict(os.environ, MOE_TC_A_IN_TMEM="1")
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    refs = L.oracle_many(h, offset=off)
+    for t in range(B):
+        check(L, h[t], y[t], idx[t], w[t], offset=off[t], ref=refs[t])
 
 
 def test_tc_two_bit_full_width():
     L = build_layer(D(FULL, bits=2), gen="device")
     h = G.hidden_states(G.SEED, 44, 8, 4096)
     y, idx, w = decode_tc(L, h)
-    for t in (0, 7):
-        check(L, h[t], y[t], idx[t], w[t])
+    refs = L.oracle_many(h)
+    for t in range(8):
+        check(L, h[t], y[t], idx[t], w[t], ref=refs[t])

@@ -1,12 +1,14 @@
 """Model check of the tensor-core contraction kernel's mbarrier protocol
 (bit_expert_matvec_moe_b300/csrc/moe_tc.cu, tc_contract_kernel): the warp
 roles are modelled as coroutines with the kernel's loop structure and its
-slot / parity arithmetic (code ring of 3, K-block ring of 4, two
-accumulators), barriers with the PTX try_wait.parity semantics and the
-kernel's arrival counts, and TMA landings and MMA commits completing in random
-order.  Every configuration must finish without a stuck wait, and every MMA
-must find the A and B blocks of its own (unit, K-block) in its slot - i.e. no
-slot is overwritten while still in use."""
+slot / parity arithmetic (code ring of 3, K-block ring of 4, a ring of 4
+accumulators each holding the partial sum of up to 4 K-blocks), barriers with
+the PTX try_wait.parity semantics and the kernel's arrival counts, and TMA
+landings and MMA commits completing in random order.  Every configuration
+must finish without a stuck wait, every MMA must find the A and B blocks of
+its own (unit, K-block) in its slot, and the epilogue must read every partial
+sum of its own (unit, span) from its accumulator - i.e. no slot or
+accumulator is overwritten while still in use."""
 import itertools
 import random
 
@@ -26,13 +28,13 @@ class Bar:
     def done(s, parity):  # try_wait.parity semantics
         return (s.phase & 1) != parity
 
-def sim(n_units, ng, kCS=3, kKS=4, D=2, seed=0):
+def sim(n_units, ng, kCS=3, kKS=4, D=4, SPAN=4, seed=0):
     rnd = random.Random(seed)
     nst = (ng + 7) // 8
     full_c = [Bar(1) for _ in range(kCS)]; empty_c = [Bar(8) for _ in range(kCS)]
     full_a = [Bar(8) for _ in range(kKS)]; full_b = [Bar(1) for _ in range(kKS)]; empty_k = [Bar(1) for _ in range(kKS)]
     dfull = [Bar(1) for _ in range(D)]; dempty = [Bar(4) for _ in range(D)]
-    smem_c = [None]*kCS; smem_a = [None]*kKS; smem_b = [None]*kKS
+    smem_c = [None]*kCS; smem_a = [None]*kKS; smem_b = [None]*kKS; tmem = [None]*D
     inflight = []  # (callback) async completions (TMA, MMA commit)
     log = {"mma": [], "epi": []}
     def producer_codes():
@@ -60,28 +62,32 @@ def sim(n_units, ng, kCS=3, kKS=4, D=2, seed=0):
                 inflight.append(land)
                 kc += 1
     def mma():
-        kc = 0; uc = 0
+        kc = 0; pc = 0
         for u in range(n_units):
-            d = uc & 1
-            while not dempty[d].done(((uc >> 1) & 1) ^ 1): yield
-            for kb in range(ng):
-                slot = kc % kKS; par = (kc // kKS) & 1
-                while not (full_a[slot].done(par) and full_b[slot].done(par)): yield
-                assert smem_a[slot] == (u, kb), (smem_a[slot], u, kb)
-                assert smem_b[slot] == (u, kb), (smem_b[slot], u, kb)
-                log["mma"].append((u, kb, d))
-                inflight.append(lambda slot=slot: empty_k[slot].arrive())
-                kc += 1
-            inflight.append(lambda d=d: dfull[d].arrive())
-            uc += 1
+            for kb0 in range(0, ng, SPAN):
+                d = pc % D
+                while not dempty[d].done(((pc // D) & 1) ^ 1): yield
+                tmem[d] = (u, kb0)
+                for kb in range(kb0, min(ng, kb0 + SPAN)):
+                    slot = kc % kKS; par = (kc // kKS) & 1
+                    while not (full_a[slot].done(par) and full_b[slot].done(par)): yield
+                    assert smem_a[slot] == (u, kb), (smem_a[slot], u, kb)
+                    assert smem_b[slot] == (u, kb), (smem_b[slot], u, kb)
+                    log["mma"].append((u, kb, d))
+                    inflight.append(lambda slot=slot: empty_k[slot].arrive())
+                    kc += 1
+                inflight.append(lambda d=d: dfull[d].arrive())
+                pc += 1
     def epi(w):
-        uc = 0
+        pc = 0
         for u in range(n_units):
-            d = uc & 1
-            while not dfull[d].done((uc >> 1) & 1): yield
-            if w == 0: log["epi"].append((u, d))
-            dempty[d].arrive()
-            uc += 1
+            for kb0 in range(0, ng, SPAN):
+                d = pc % D
+                while not dfull[d].done((pc // D) & 1): yield
+                assert tmem[d] == (u, kb0), (tmem[d], u, kb0)
+                if w == 0: log["epi"].append((u, kb0, d))
+                dempty[d].arrive()
+                pc += 1
     def deq(w):
         cc = 0; kc = 0
         for u in range(n_units):
@@ -111,7 +117,7 @@ def sim(n_units, ng, kCS=3, kKS=4, D=2, seed=0):
         if not alive and not inflight: break
         idle = 0 if progressed else idle + 1
         if idle > 2000 and not inflight: return False, log
-    assert len(log["mma"]) == n_units * ng and len(log["epi"]) == n_units
+    assert len(log["mma"]) == n_units * ng and len(log["epi"]) == n_units * ((ng + SPAN - 1) // SPAN)
     return True, log
 
 
