@@ -75,7 +75,7 @@ WsLayout ws_layout(const moe_dims& d, int B) {
   // depend on the batch (epoch << 32 | value)
   L.pub_logits = take((size_t)(MOE_MAX_EXPERTS + 1) * 8);
   L.pub_act = take(ns * I * 8);
-  L.logits = take(B * (E + 1) * 4);
+  L.logits = take((size_t)router_splits(B, (int)H, (int)E) * B * (E + 1) * 4);
   L.idx = take(B * K * 4);
   L.w = take(B * K * 4);
   L.gs = take(B * 4);
@@ -257,12 +257,15 @@ moe_status moe_route(const moe_dims* dims, const float* xn, int32_t B, const uin
   r.E = dims->n_experts;
   r.router = router;
   r.gate = nullptr;
-  r.offset = logit_offset;
+  r.stages_per_split = router_stages_per_split(B, r.H, r.E);
   r.logits = at<float>(ws, L.logits);
   cudaError_t e = launch_router(r, s);
   if (e != cudaSuccess) return cuda_fail(e);
   TopkArgs t{};
   t.logits = r.logits;
+  t.offset = logit_offset;
+  t.B = B;
+  t.splits = router_splits(B, r.H, r.E);
   t.E = dims->n_experts;
   t.K = dims->top_k;
   t.has_gate = 0;
@@ -462,12 +465,15 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   r.E = E;
   r.router = layer->router;
   r.gate = has_gate ? layer->shared_gate : nullptr;
-  r.offset = logit_offset;
+  r.stages_per_split = router_stages_per_split(B, H, E);
   r.logits = at<float>(ws, L.logits);
   if ((e = launch_router(r, s)) != cudaSuccess) return cuda_fail(e);
 
   TopkArgs t{};
   t.logits = r.logits;
+  t.offset = logit_offset;
+  t.B = B;
+  t.splits = router_splits(B, H, E);
   t.E = E;
   t.K = K;
   t.has_gate = has_gate;

@@ -40,14 +40,16 @@ struct NormQuantArgs {
 struct RouterArgs {
   const float* xn;
   int B, H, E;
+  int stages_per_split;  // router_stages_per_split(B, H, E)
   const uint16_t* router;
   const uint16_t* gate;  // extra row E, or null
-  const float* offset;   // [B, E] or null
-  float* logits;         // [B, E + 1]
+  float* logits;         // partial sums [splits][B][E + 1]
 };
 
 struct TopkArgs {
-  const float* logits;  // [B, E + 1]
+  const float* logits;  // router partial sums [splits][B][E + 1]
+  const float* offset;  // [B, E] or null
+  int B, splits;
   int E, K, has_gate;
   int32_t* idx;
   float* w;
@@ -148,6 +150,9 @@ struct DecodeArgs {
 
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t s);
 cudaError_t launch_norm_quant(const NormQuantArgs& a, int B, cudaStream_t s);
+// Router splits of the input dimension: a function of the shape only.
+int router_splits(int B, int H, int E);
+int router_stages_per_split(int B, int H, int E);
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, int B, cudaStream_t s);
 cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t s);

@@ -117,59 +117,137 @@ __global__ void __launch_bounds__(kBlock) norm_quant_kernel(NormQuantArgs a) {
 // router matvec: logits[b][e] = router[e] . xn[b] (+ offset[b][e]); row E is the
 // shared-expert gate vector when present (no offset)
 // ---------------------------------------------------------------------------
-// Tiled over (router rows, tokens): a block computes kRtRows rows x kRtTok
-// tokens, staging chunks of kRtK inputs of the rows (bf16) and of the tokens'
-// xn (fp32) in shared memory (rows padded by one word against bank
-// conflicts).  Four adjacent threads share one output, each taking every
-// fourth input pair with two interleaved partial sums; the four are combined by
-// shuffles in a fixed order, so results do not depend on scheduling and
-// rounding chains stay short.
-constexpr int kRtRows = 8, kRtTok = 8, kRtK = 256, kRtSplit = 4;
-static_assert(kRtRows * kRtTok * kRtSplit == 256, "router block shape");
-__global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
-  __shared__ float xs[kRtTok][kRtK + 1];
-  __shared__ uint32_t rs[kRtRows][kRtK / 2 + 1];  // bf16 pairs
+// Register-tiled fp32 product over (router rows, tokens, input splits).  A block
+// owns kRtRows rows x TOK tokens and one contiguous range of the inputs; each
+// thread holds an RT x TT tile of sums.  Stages of kRtK inputs are read into
+// registers one stage ahead, then written to shared memory k-major (the rows
+// converted from bf16 to fp32 on the way) so that one vector load per operand
+// feeds the RT x TT fused multiply-adds of one input.  Every sum runs over its
+// inputs in ascending order; the top-K kernel adds the splits' partial sums in
+// ascending split order, so results do not depend on scheduling.
+constexpr int kRtRows = 64, kRtK = 32, kRtThreads = 256;
+constexpr int kRtTargetBlocks = 2 * 148;  // a fixed shape-only target: results do not depend on the device
+constexpr int kRtMaxSplits = 32;
+
+static int router_tok_tile(int B) { return B <= 16 ? 16 : (B <= 32 ? 32 : 64); }
+
+int router_splits(int B, int H, int E) {
+  const int tiles = ((E + 1 + kRtRows - 1) / kRtRows) * ((B + router_tok_tile(B) - 1) / router_tok_tile(B));
+  const int stages = H / kRtK;
+  const int want = std::min(std::min(kRtMaxSplits, stages), std::max(1, (kRtTargetBlocks + tiles - 1) / tiles));
+  const int per = (stages + want - 1) / want;
+  return (stages + per - 1) / per;
+}
+
+template <int N>
+__device__ __forceinline__ void load_vec(const float* p, float (&v)[N]) {
+  static_assert(N == 2 || N == 4, "vector width");
+  if constexpr (N == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    v[0] = t.x; v[1] = t.y;
+  }
+}
+
+template <int RT, int TT, int TX>
+__global__ void __launch_bounds__(kRtThreads) router_kernel(RouterArgs a) {
+  constexpr int TR = kRtThreads / TX, TOK = TT * TX;
+  static_assert(RT * TR == kRtRows, "router row tile");
+  constexpr int WSTR = kRtRows + 4, XSTR = TOK + 4;  // k-major strides (16-byte multiples)
+  constexpr int WV = kRtRows * kRtK / 8 / kRtThreads;     // 16-byte row pieces per thread
+  constexpr int XN = TOK * kRtK / 4;                      // 16-byte token pieces per stage
+  constexpr int XV = (XN + kRtThreads - 1) / kRtThreads;
+  __shared__ __align__(16) float ws[2][kRtK][WSTR];
+  __shared__ __align__(16) float xs[2][kRtK][XSTR];
   const int tid = threadIdx.x;
+  const int tx = tid % TX, tr = tid / TX;
   const int nrows = a.E + (a.gate ? 1 : 0);
-  const int row0 = blockIdx.x * kRtRows, b0 = blockIdx.y * kRtTok;
-  const int o = tid / kRtSplit, q = tid % kRtSplit;  // output o: row o / kRtTok, token o % kRtTok
-  const int lr = o / kRtTok, lt = o % kRtTok;
-  float acc = 0.f;
-  for (int k0 = 0; k0 < a.H; k0 += kRtK) {
-    const int kn = min(kRtK, a.H - k0);  // a multiple of 64
-    for (int i = tid; i < kRtTok * (kn / 4); i += 256) {
-      const int t = i / (kn / 4), c = 4 * (i - t * (kn / 4));
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (b0 + t < a.B) v = *reinterpret_cast<const float4*>(a.xn + (size_t)(b0 + t) * a.H + k0 + c);
-      xs[t][c] = v.x; xs[t][c + 1] = v.y; xs[t][c + 2] = v.z; xs[t][c + 3] = v.w;
-    }
-    for (int i = tid; i < kRtRows * (kn / 8); i += 256) {
-      const int r = i / (kn / 8), c = 8 * (i - r * (kn / 8));
+  const int row0 = blockIdx.x * kRtRows, b0 = blockIdx.y * TOK;
+  const int s0 = blockIdx.z * a.stages_per_split, s1 = min(a.H / kRtK, s0 + a.stages_per_split);
+
+  uint4 wr[WV];
+  float4 xr[XV];
+  auto fetch = [&](int st) {
+    const int k0 = st * kRtK;
+#pragma unroll
+    for (int v = 0; v < WV; ++v) {
+      const int i = tid + kRtThreads * v, r = i >> 2, c = i & 3;
       const int row = row0 + r;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      wr[v] = make_uint4(0u, 0u, 0u, 0u);
       if (row < nrows) {
         const uint16_t* R = row < a.E ? a.router + (size_t)row * a.H : a.gate;
-        v = *reinterpret_cast<const uint4*>(R + k0 + c);
+        wr[v] = __ldg(reinterpret_cast<const uint4*>(R + k0 + 8 * c));
       }
-      rs[r][c / 2] = v.x; rs[r][c / 2 + 1] = v.y; rs[r][c / 2 + 2] = v.z; rs[r][c / 2 + 3] = v.w;
     }
-    __syncthreads();
-    float p0 = 0.f, p1 = 0.f;
-    for (int c = q; c < kn / 2; c += 2 * kRtSplit) {  // pairs c and c + kRtSplit (kn / 2 is a multiple of 8)
-      const uint32_t w0 = rs[lr][c], w1 = rs[lr][c + kRtSplit];
-      p0 = fmaf(bf16hi(w0), xs[lt][2 * c + 1], fmaf(bf16lo(w0), xs[lt][2 * c], p0));
-      p1 = fmaf(bf16hi(w1), xs[lt][2 * (c + kRtSplit) + 1], fmaf(bf16lo(w1), xs[lt][2 * (c + kRtSplit)], p1));
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+      const int i = tid + kRtThreads * v, t = i >> 3, c = i & 7;
+      xr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < XN && b0 + t < a.B) xr[v] = *reinterpret_cast<const float4*>(a.xn + (size_t)(b0 + t) * a.H + k0 + 4 * c);
     }
-    acc += p0 + p1;
+  };
+  auto stash = [&](int buf) {
+#pragma unroll
+    for (int v = 0; v < WV; ++v) {
+      const int i = tid + kRtThreads * v, r = i >> 2, c = i & 3;
+      const uint32_t w4[4] = {wr[v].x, wr[v].y, wr[v].z, wr[v].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        ws[buf][8 * c + 2 * j][r] = bf16lo(w4[j]);
+        ws[buf][8 * c + 2 * j + 1][r] = bf16hi(w4[j]);
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+      const int i = tid + kRtThreads * v, t = i >> 3, c = i & 7;
+      if (i < XN) {
+        xs[buf][4 * c][t] = xr[v].x;
+        xs[buf][4 * c + 1][t] = xr[v].y;
+        xs[buf][4 * c + 2][t] = xr[v].z;
+        xs[buf][4 * c + 3][t] = xr[v].w;
+      }
+    }
+  };
+
+  float acc[RT][TT];
+#pragma unroll
+  for (int i = 0; i < RT; ++i)
+#pragma unroll
+    for (int j = 0; j < TT; ++j) acc[i][j] = 0.f;
+  if (s0 < s1) {
+    fetch(s0);
+    stash(0);
+  }
+  __syncthreads();
+  for (int st = s0; st < s1; ++st) {
+    const int buf = (st - s0) & 1;
+    if (st + 1 < s1) fetch(st + 1);
+#pragma unroll 8
+    for (int k = 0; k < kRtK; ++k) {
+      float w[RT], x[TT];
+      load_vec<RT>(&ws[buf][k][tr * RT], w);
+      load_vec<TT>(&xs[buf][k][tx * TT], x);
+#pragma unroll
+      for (int i = 0; i < RT; ++i)
+#pragma unroll
+        for (int j = 0; j < TT; ++j) acc[i][j] = fmaf(w[i], x[j], acc[i][j]);
+    }
+    if (st + 1 < s1) stash(buf ^ 1);
     __syncthreads();
   }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-  const int row = row0 + lr, b = b0 + lt;
-  if (q == 0 && row < nrows && b < a.B) {
-    float v = acc;
-    if (row < a.E && a.offset) v += a.offset[(size_t)b * a.E + row];
-    a.logits[(size_t)b * (a.E + 1) + row] = v;
+  // partial sums of this split: logits[split][token][row]
+  float* out = a.logits + (size_t)blockIdx.z * a.B * (a.E + 1);
+#pragma unroll
+  for (int j = 0; j < TT; ++j) {
+    const int b = b0 + tx * TT + j;
+    if (b >= a.B) continue;
+#pragma unroll
+    for (int i = 0; i < RT; ++i) {
+      const int row = row0 + tr * RT + i;
+      if (row < nrows) out[(size_t)b * (a.E + 1) + row] = acc[i][j];
+    }
   }
 }
 
@@ -177,9 +255,24 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 // softmax / top-K / renormalise per token: one warp per token
 // ---------------------------------------------------------------------------
 constexpr int kTopkPer = 32;  // experts per lane: up to 1024 experts
-__global__ void __launch_bounds__(32) topk_kernel(TopkArgs a) {
-  const int b = blockIdx.x, lane = threadIdx.x;
-  const float* lg = a.logits + (size_t)b * (a.E + 1);
+constexpr int kTopkThreads = 256;
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  // logits of this token: the router's split partial sums added in split order,
+  // then the caller's offset (routed experts only)
+  __shared__ float s_lg[kTopkPer * 32 + 1];
+  const size_t pstride = (size_t)a.B * (a.E + 1);
+  const float* part = a.logits + (size_t)b * (a.E + 1);
+  const int nrows = a.E + (a.has_gate ? 1 : 0);
+  for (int e = tid; e < nrows; e += blockDim.x) {
+    float v = part[e];
+    for (int sp = 1; sp < a.splits; ++sp) v += part[sp * pstride + e];
+    if (e < a.E && a.offset) v += a.offset[(size_t)b * a.E + e];
+    s_lg[e] = v;
+  }
+  __syncthreads();
+  if (tid >= 32) return;
+  const float* lg = s_lg;
   uint32_t key[kTopkPer];
   bool finite = true;
 #pragma unroll
@@ -523,12 +616,24 @@ cudaError_t launch_norm_quant(const NormQuantArgs& a, int B, cudaStream_t s) {
 }
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   const int rows = a.E + (a.gate ? 1 : 0);
-  dim3 grid((rows + kRtRows - 1) / kRtRows, (a.B + kRtTok - 1) / kRtTok);
-  router_kernel<<<grid, 256, 0, s>>>(a);
+  const int tok = router_tok_tile(a.B);
+  const int splits = (a.H / kRtK + a.stages_per_split - 1) / a.stages_per_split;
+  if (a.stages_per_split < 1 || splits != router_splits(a.B, a.H, a.E)) return cudaErrorInvalidValue;
+  dim3 grid((rows + kRtRows - 1) / kRtRows, (a.B + tok - 1) / tok, splits);
+  if (tok == 16)
+    router_kernel<2, 2, 8><<<grid, kRtThreads, 0, s>>>(a);
+  else if (tok == 32)
+    router_kernel<4, 2, 16><<<grid, kRtThreads, 0, s>>>(a);
+  else
+    router_kernel<4, 4, 16><<<grid, kRtThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
+int router_stages_per_split(int B, int H, int E) {
+  const int stages = H / kRtK, sp = router_splits(B, H, E);
+  return (stages + sp - 1) / sp;
+}
 cudaError_t launch_topk(const TopkArgs& a, int B, cudaStream_t s) {
-  topk_kernel<<<B, 32, 0, s>>>(a);
+  topk_kernel<<<B, kTopkThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t s) {
