@@ -14,15 +14,26 @@
 // Contraction (tc_contract_kernel, persistent, one 480-thread CTA per SM):
 //   warp 0     TMA producer: per unit, the code pieces and (scale, bias) words
 //              of 8 groups x 128 rows per stage (3 stages in flight);
-//   warp 1     TMA producer: per K-block (64 inputs) the entry rows of B;
-//   warp 2     owns the tensor memory (a ring of 4 accumulators of 64
-//              columns) and issues 4 MMAs (M 128, N 2 x tokens, K 16) per
-//              K-block, starting a fresh accumulator every kSpanKB K-blocks;
+//   warp 1     TMA producer: per K-block (64 inputs) the entry rows of B into
+//              shared memory (8 K-blocks in flight);
+//   warp 2     owns the tensor memory (a ring of 4 accumulators of 64 columns,
+//              then one 32-column A block per K slot) and issues, from one
+//              elected lane of a warp that walks the work list in step, 4 MMAs
+//              (M 128, N 2 x tokens, K 16, A in tensor memory) per K-block,
+//              two K-blocks per round of waits, starting a fresh accumulator
+//              every kSpanKB K-blocks;
 //   warps 3-6  epilogue: add up a unit's partial sums in fp32 registers
 //              (one warp per tensor-memory lane quarter), then add hi and lo
 //              columns, scale, SwiGLU for gate/up, store;
-//   warps 7-14 dequantise the staged codes into the A operand (fp16
-//              q*s + b, 128-byte swizzled) of 4 K-blocks in flight.
+//   warps 7-14 dequantise the staged codes (fp16 q*s + b) straight into the
+//              tensor-memory A blocks: two warps per lane quarter, one taking
+//              the even and one the odd K-blocks, each all 64 inputs of its
+//              32 rows.
+// Waits first test the barrier phase (mbarrier.test_wait, cheap when it has
+// already completed) and only then poll with try_wait.  Measured on B300 with
+// the 128-token batch: a completed-phase try_wait cost about 170 cycles inside
+// the MMA loop, a test_wait about 50; per-MMA descriptor work in a one-lane
+// branch cost about 60 cycles an MMA against 45 from a warp-uniform loop.
 // Every wait is bounded (1 s); a CTA that gives up records ST_TIMEOUT, lets
 // its copies and MMAs in flight finish (bounded), frees its tensor memory and
 // returns.  Units are taken round-robin (unit = CTA, CTA + grid, ...), so the
@@ -177,9 +188,24 @@ __device__ __forceinline__ void dequant_word2(uint32_t w, __half2 s, __half2 b, 
 // ---------------------------------------------------------------------------
 // the contraction
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{ .reg .pred p; elect.sync _|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(pred));
+  return pred != 0;
+}
 // Bounded mbarrier wait that also gives up once another role of the CTA has.
+// A phase that has already completed is seen by test_wait (non-blocking, a few
+// tens of cycles); try_wait, which may suspend the thread, only after that.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+               : "=r"(ok)
+               : "r"(su32(bar)), "r"(parity)
+               : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort) return false;
@@ -227,7 +253,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&empty_c[i], 8);
     }
     for (int i = 0; i < kKSlots; ++i) {
-      mbar_init(&full_a[i], 8);
+      mbar_init(&full_a[i], 4);
       mbar_init(&full_b[i], 1);
       mbar_init(&empty_k[i], 1);
     }
@@ -299,7 +325,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kb = 0; kb < a.ng; ++kb, ++kc) {
           const uint32_t slot = kc % kKSlots;
           if (!(ok = tc_wait(&empty_k[slot], ((kc / kKSlots) & 1u) ^ 1u, abort))) break;
-          uint8_t* dst = sm + kOffK + slot * kKSlotBytes + kABytes;
+          uint8_t* dst = sm + kOffK + slot * kKSlotBytes;
           mbar_expect_tx(&full_b[slot], (uint32_t)boxes * kBBoxBytes);
           for (int i = 0; i < boxes; ++i)
             tma_load_2d(dst + i * kBBoxBytes, &m_b, kb * 64, 2 * ch.e0 + (int)kBBoxRows * i, &full_b[slot]);
@@ -310,35 +336,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ---- MMAs ---------------------------------------------------------------
-    // Partial sums: a fresh accumulator (ring slot pc % kDBufs) every kSpanKB
-    // K-blocks of a unit, committed to dfull for the epilogue.
-    if (lane == 0) {
-      uint32_t kc = 0, pc = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const TcChunk ch = a.chunks[u / a.tiles];
-        const uint32_t idesc = make_idesc_f16(kTcM, 2 * ((ch.n + 7) & ~7));
-        for (int kb0 = 0; kb0 < a.ng && ok; kb0 += kSpanKB, ++pc) {
-          const uint32_t d = pc % kDBufs;
-          if (!(ok = tc_wait(&dempty[d], ((pc / kDBufs) & 1u) ^ 1u, abort))) break;
-          tc_fence_after();
-          const uint32_t dt = tmem + d * kDCols;
-          const int kb1 = min(a.ng, kb0 + kSpanKB);
-          for (int kb = kb0; kb < kb1; ++kb, ++kc) {
-            const uint32_t slot = kc % kKSlots, par = (kc / kKSlots) & 1u;
-            if (!(ok = tc_wait(&full_a[slot], par, abort) && tc_wait(&full_b[slot], par, abort))) break;
-            tc_fence_after();
-            const uint32_t aa = su32(sm + kOffK + slot * kKSlotBytes), ba = aa + kABytes;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(dt, sdesc_sw128_kmajor(aa + 32 * kk), sdesc_sw128_kmajor(ba + 32 * kk), idesc,
-                         (kb != kb0 || kk != 0) ? 1u : 0u);
-            mma_commit(&empty_k[slot]);
+    // The whole warp walks the work list (so every operand below is
+    // warp-uniform); one elected lane issues the MMAs and commits.  Partial
+    // sums: a fresh accumulator (ring slot pc % kDBufs) every kSpanKB K-blocks
+    // of a unit, committed to dfull for the epilogue.
+    uint32_t kc = 0, pc = 0;
+    bool ok = true;
+    const uint64_t bdesc0 = sdesc_sw128_kmajor(su32(sm + kOffK));
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const TcChunk ch = a.chunks[u / a.tiles];
+      const uint32_t idesc = make_idesc_f16(kTcM, 2 * ((ch.n + 7) & ~7));
+      for (int kb0 = 0; kb0 < a.ng && ok; kb0 += kSpanKB, ++pc) {
+        const uint32_t d = pc % kDBufs;
+        if (!(ok = __all_sync(0xffffffffu, lane != 0 || tc_wait(&dempty[d], ((pc / kDBufs) & 1u) ^ 1u, abort)))) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + d * kDCols;
+        const int kb1 = min(a.ng, kb0 + kSpanKB);
+        // K-blocks in pairs: one round of waits, then up to 8 MMAs
+        for (int kb = kb0, nkb = 0; kb < kb1; kb += nkb, kc += nkb) {
+          nkb = min(2, kb1 - kb);
+          bool w = true;
+          if (lane == 0) {
+            for (int i = 0; i < nkb && w; ++i) {
+              const uint32_t sl = (kc + i) % kKSlots, pa = ((kc + i) / kKSlots) & 1u;
+              w = tc_wait(&full_a[sl], pa, abort) && tc_wait(&full_b[sl], pa, abort);
+            }
           }
-          if (ok) mma_commit(&dfull[d]);
+          if (!(ok = __all_sync(0xffffffffu, w))) break;
+          tc_fence_after();
+          if (elect_one()) {
+            for (int i = 0; i < nkb; ++i) {
+              const uint32_t slot = (kc + i) % kKSlots;
+              const uint64_t bd = bdesc0 + (uint64_t)(slot * (kKSlotBytes >> 4));
+              const uint32_t at = tmem + kTmemACol0 + slot * 32;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ts(dt, at + 8 * kk, bd + 2 * kk, idesc, (kb + i != kb0 || kk != 0) ? 1u : 0u);
+              mma_commit(&empty_k[slot]);
+            }
+          }
+          __syncwarp();
         }
+        if (ok && elect_one()) mma_commit(&dfull[d]);
+        __syncwarp();
       }
-      // every MMA issued by this CTA has finished reading shared memory
+    }
+    // every MMA issued by this CTA has finished reading its operands
+    if (elect_one()) {
       mma_commit(drain);
       mbar_wait(drain, 0);
     }
@@ -410,40 +454,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t cs = cc % kCodeSlots;
         if (!(ok = tc_wait_warp(&full_c[cs], (cc / kCodeSlots) & 1u, abort))) break;
         const uint8_t* cb = sm + kOffCodes + cs * kCodeSlotBytes;
-        const uint4 sb0 = *reinterpret_cast<const uint4*>(cb + 2 * kHalfBoxBytes + r * 32);
-        const uint4 sb1 = *reinterpret_cast<const uint4*>(cb + 2 * kHalfBoxBytes + r * 32 + 16);
-        const uint32_t sbw[8] = {sb0.x, sb0.y, sb0.z, sb0.w, sb1.x, sb1.y, sb1.z, sb1.w};
         const int gcount = min(kStageGroups, a.ng - kStageGroups * st);
-#pragma unroll
-        for (int j = 0; j < kStageGroups; ++j) {
-          if (j >= gcount) break;
-          const uint32_t ks = kc % kKSlots;
-          if (!(ok = tc_wait_warp(&empty_k[ks], ((kc / kKSlots) & 1u) ^ 1u, abort))) break;
-          const float s = bf16lo(sbw[j]), b = bf16hi(sbw[j]);
+        // this warp takes the K-blocks kc + j with (kc + j) % 2 == h, all 64
+        // inputs of its 32 rows: with an even ring every K slot then has one
+        // writer per lane quarter, which keeps the slot parities exact
+#pragma unroll 1
+        for (int j = h ^ (int)(kc & 1u); j < gcount; j += 2) {
+          const uint32_t kj = kc + j, ks = kj % kKSlots;
+          if (!(ok = tc_wait_warp(&empty_k[ks], ((kj / kKSlots) & 1u) ^ 1u, abort))) break;
+          const uint32_t sbj = *reinterpret_cast<const uint32_t*>(cb + 2 * kHalfBoxBytes + r * 32 + 4 * j);
+          const float s = bf16lo(sbj), b = bf16hi(sbj);
           bad |= !(fabsf(s) * qmax + fabsf(b) <= 65504.f);
           const __half2 s2 = __float2half2_rn(s), b2 = __float2half2_rn(b);
-          uint4 c0, c1, c2, c3;  // chunks 4h .. 4h+3 of this row's K-block
+          uint32_t v[32];
           if (ch.bits == 4) {
-            const uint4 c = *reinterpret_cast<const uint4*>(cb + h * kHalfBoxBytes + swz128(r, j));
-            c0 = dequant_word4(c.x, s2, b2);
-            c1 = dequant_word4(c.y, s2, b2);
-            c2 = dequant_word4(c.z, s2, b2);
-            c3 = dequant_word4(c.w, s2, b2);
+            const uint4 c = *reinterpret_cast<const uint4*>(cb + swz128(r, j));
+            const uint4 d = *reinterpret_cast<const uint4*>(cb + kHalfBoxBytes + swz128(r, j));
+            const uint32_t w8[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint4 o = dequant_word4(w8[i], s2, b2);
+              v[4 * i] = o.x; v[4 * i + 1] = o.y; v[4 * i + 2] = o.z; v[4 * i + 3] = o.w;
+            }
           } else {
-            const uint2 c = *reinterpret_cast<const uint2*>(cb + swz128(r, j) + 8 * h);
-            dequant_word2(c.x, s2, b2, c0, c1);
-            dequant_word2(c.y, s2, b2, c2, c3);
+            const uint4 c = *reinterpret_cast<const uint4*>(cb + swz128(r, j));
+            const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 o0, o1;
+              dequant_word2(w4[i], s2, b2, o0, o1);
+              v[8 * i] = o0.x; v[8 * i + 1] = o0.y; v[8 * i + 2] = o0.z; v[8 * i + 3] = o0.w;
+              v[8 * i + 4] = o1.x; v[8 * i + 5] = o1.y; v[8 * i + 6] = o1.z; v[8 * i + 7] = o1.w;
+            }
           }
-          uint8_t* A = sm + kOffK + ks * kKSlotBytes;
-          *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 0)) = c0;
-          *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 1)) = c1;
-          *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 2)) = c2;
-          *reinterpret_cast<uint4*>(A + swz128(r, 4 * h + 3)) = c3;
-          fence_proxy_async();  // generic-proxy writes -> visible to the MMA (async proxy)
+          tc_fence_after();  // the MMAs that read this slot have completed (empty_k)
+          const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemACol0 + ks * 32;
+          tmem_st16(ta, *reinterpret_cast<const uint32_t(*)[16]>(&v[0]));
+          tmem_st16(ta + 16, *reinterpret_cast<const uint32_t(*)[16]>(&v[16]));
+          tmem_st_wait();
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&full_a[ks]);
-          ++kc;
         }
+        kc += gcount;
         if (!ok) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_c[cs]);

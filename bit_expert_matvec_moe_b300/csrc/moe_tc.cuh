@@ -62,15 +62,17 @@ constexpr int kTcM = 128;            // weight rows per tile (MMA M)
 constexpr int kTcTok = 32;           // tokens per unit at most (MMA N = 2 * tokens <= 64)
 constexpr int kStageGroups = 8;      // groups per code stage (one TMA box = 128 bytes of codes per row)
 constexpr int kCodeSlots = 3;        // code stages in flight
-constexpr int kKSlots = 4;           // K-blocks (A + B operands) in flight
+constexpr int kKSlots = 8;           // K-blocks in flight (A in tensor memory, B in shared memory)
 constexpr int kSpanKB = 4;           // K-blocks summed in one accumulator before the epilogue takes it
 constexpr int kDBufs = 4;            // accumulators in tensor memory (a ring of partial sums)
 constexpr int kDCols = 64;           // tensor-memory columns per accumulator (N <= 64)
-constexpr int kTmemCols = kDBufs * kDCols;  // allocation (power of two >= 32)
+constexpr int kTmemACol0 = kDBufs * kDCols;  // A operand: one 32-column block (64 fp16 per lane) per K slot
+constexpr int kTmemCols = 512;               // allocation (power of two >= 32)
+static_assert(kTmemACol0 + kKSlots * 32 <= kTmemCols, "tensor-memory plan");
 
-constexpr uint32_t kABytes = kTcM * 128;               // 16 KB: one K-block of A
+constexpr uint32_t kABytes = kTcM * 128;               // 16 KB: one K-block of A (in tensor memory: 32 columns)
 constexpr uint32_t kBBytes = 2 * kTcTok * 128;          // 8 KB: one K-block of B at N = 64
-constexpr uint32_t kKSlotBytes = kABytes + kBBytes;     // 24 KB
+constexpr uint32_t kKSlotBytes = kBBytes;              // 8 KB: B only (A lives in tensor memory)
 constexpr uint32_t kHalfBoxBytes = kTcM * 128;          // 16 KB: 8 groups' 16-byte code pieces x 128 rows
 constexpr uint32_t kSbBoxBytes = kTcM * 32;             // 4 KB: 8 groups' (scale, bias) words x 128 rows
 constexpr uint32_t kCodeSlotBytes = 2 * kHalfBoxBytes + kSbBoxBytes;  // 36 KB
@@ -232,6 +234,26 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T: A in tensor memory, row m in lane m, two
+// consecutive fp16 of K per 32-bit column
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 16 consecutive 32-bit columns of this warp's 32 lanes, written from registers
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // arrive once on an mbarrier when every MMA issued so far by this thread is done
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))

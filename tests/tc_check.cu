@@ -171,7 +171,9 @@ int main() {
   }
 
   // shared-memory plan
-  CHECK(kOffCodes % 1024 == 0 && kKSlotBytes % 1024 == 0 && kABytes % 1024 == 0, "A / B alignment");
+  CHECK(kOffCodes % 1024 == 0 && kKSlotBytes % 1024 == 0, "B slot alignment");
+  CHECK(kTmemACol0 >= kDBufs * kDCols && kTmemACol0 + kKSlots * 32 <= kTmemCols, "A blocks after the accumulators");
+  CHECK(kKSlots % 2 == 0, "even K ring: one writer per slot and lane quarter");
   CHECK(kCodeSlotBytes % 1024 == 0 && kHalfBoxBytes % 1024 == 0, "code box alignment");
   CHECK(kOffBars % 8 == 0 && kOffBars >= kOffCodes + kCodeSlots * kCodeSlotBytes, "barriers after the code slots");
   CHECK(kOffMisc + 12 <= kSmemUsed && kSmemBytes <= 232448, "plan total");

@@ -54,14 +54,14 @@ def decode_tc(L, h_np, offset=None, tc=True):
     return h.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
 
 
-def check(L, h_tok, y, idx, w, offset=None, ref=None):
+def check(L, h_tok, y, idx, w, offset=None, ref=None, delta_tol=REL_TOL):
     ref = L.oracle(h_tok, offset=offset) if ref is None else ref
     ok, tie = routing_ok(idx, ref["logits"], L.dims.top_k)
     assert ok
     if tie:
         ref = L.oracle(h_tok, offset=offset, force_chosen=idx)
     assert rel_err(y, ref["y"]) <= REL_TOL, rel_err(y, ref["y"])
-    assert rel_err(y - h_tok, ref["y"] - h_tok) <= REL_TOL, rel_err(y - h_tok, ref["y"] - h_tok)
+    assert rel_err(y - h_tok, ref["y"] - h_tok) <= delta_tol, rel_err(y - h_tok, ref["y"] - h_tok)
 
 
 @pytest.mark.parametrize("bits", [4, 2])
@@ -132,6 +132,27 @@ def test_tc_edge_shapes(variant):
     y, idx, w = decode_tc(L, h)
     for t in (0, 5):
         check(L, h[t], y[t], idx[t], w[t])
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_tc_odd_group_counts_many_units(bits):
+    """5 groups along hidden and 3 along inter, 64 experts and 64 tokens: more
+    units than CTAs, so a CTA's K-block count crosses odd unit boundaries (the
+    dequantising warps split K-blocks by their parity over the whole launch)."""
+    d = D(dict(hidden=320, inter=192, n_experts=64, top_k=4), bits=bits)
+    L = build_layer(d, shared_bits=bits)
+    B = 64
+    h = G.hidden_states(G.SEED, 45, B, 320)
+    y, idx, w = decode_tc(L, h)
+    y2, idx2, w2 = decode_tc(L, h, tc=False)
+    assert (idx == idx2).all()
+    refs = L.oracle_many(h)
+    # The layer output meets the bar; its MoE part alone (output minus the
+    # residual) gets 4e-3 at 2 bits: the A operand holds each weight q*s + b
+    # rounded to fp16 (relative 2^-11) and a 320-input sum averages few of them.
+    delta_tol = REL_TOL if bits == 4 else 4e-3
+    for t in range(B):
+        check(L, h[t], y[t], idx[t], w[t], ref=refs[t], delta_tol=delta_tol)
 
 
 @pytest.mark.parametrize("B", [8, 64])

@@ -1,9 +1,12 @@
 """Model check of the tensor-core contraction kernel's mbarrier protocol
 (bit_expert_matvec_moe_b300/csrc/moe_tc.cu, tc_contract_kernel): the warp
 roles are modelled as coroutines with the kernel's loop structure and its
-slot / parity arithmetic (code ring of 3, K-block ring of 4, a ring of 4
-accumulators each holding the partial sum of up to 4 K-blocks), barriers with
-the PTX try_wait.parity semantics and the kernel's arrival counts, and TMA
+slot / parity arithmetic (code ring of 3, K-block ring of 8, a ring of 4
+accumulators each holding the partial sum of up to 4 K-blocks; the MMA warp
+takes K-blocks in pairs; the two dequantising warps of each tensor-memory lane
+quarter take the even and the odd K-blocks, counted over the whole launch so
+that every K slot has one writer per quarter), barriers with the PTX
+test_wait / try_wait.parity semantics and the kernel's arrival counts, and TMA
 landings and MMA commits completing in random order.  Every configuration
 must finish without a stuck wait, every MMA must find the A and B blocks of
 its own (unit, K-block) in its slot, and the epilogue must read every partial
@@ -28,13 +31,13 @@ class Bar:
     def done(s, parity):  # try_wait.parity semantics
         return (s.phase & 1) != parity
 
-def sim(n_units, ng, kCS=3, kKS=4, D=4, SPAN=4, seed=0):
+def sim(n_units, ng, kCS=3, kKS=8, D=4, SPAN=4, PAIR=2, seed=0, stage_parity=False):
     rnd = random.Random(seed)
     nst = (ng + 7) // 8
     full_c = [Bar(1) for _ in range(kCS)]; empty_c = [Bar(8) for _ in range(kCS)]
-    full_a = [Bar(8) for _ in range(kKS)]; full_b = [Bar(1) for _ in range(kKS)]; empty_k = [Bar(1) for _ in range(kKS)]
+    full_a = [Bar(4) for _ in range(kKS)]; full_b = [Bar(1) for _ in range(kKS)]; empty_k = [Bar(1) for _ in range(kKS)]
     dfull = [Bar(1) for _ in range(D)]; dempty = [Bar(4) for _ in range(D)]
-    smem_c = [None]*kCS; smem_a = [None]*kKS; smem_b = [None]*kKS; tmem = [None]*D
+    smem_c = [None]*kCS; smem_a = [[None]*4 for _ in range(kKS)]; smem_b = [None]*kKS; tmem = [None]*D
     inflight = []  # (callback) async completions (TMA, MMA commit)
     log = {"mma": [], "epi": []}
     def producer_codes():
@@ -68,14 +71,20 @@ def sim(n_units, ng, kCS=3, kKS=4, D=4, SPAN=4, seed=0):
                 d = pc % D
                 while not dempty[d].done(((pc // D) & 1) ^ 1): yield
                 tmem[d] = (u, kb0)
-                for kb in range(kb0, min(ng, kb0 + SPAN)):
-                    slot = kc % kKS; par = (kc // kKS) & 1
-                    while not (full_a[slot].done(par) and full_b[slot].done(par)): yield
-                    assert smem_a[slot] == (u, kb), (smem_a[slot], u, kb)
-                    assert smem_b[slot] == (u, kb), (smem_b[slot], u, kb)
-                    log["mma"].append((u, kb, d))
-                    inflight.append(lambda slot=slot: empty_k[slot].arrive())
-                    kc += 1
+                kb1 = min(ng, kb0 + SPAN)
+                kb = kb0
+                while kb < kb1:
+                    nkb = min(PAIR, kb1 - kb)
+                    for i in range(nkb):
+                        slot = (kc + i) % kKS; par = ((kc + i) // kKS) & 1
+                        while not (full_a[slot].done(par) and full_b[slot].done(par)): yield
+                    for i in range(nkb):
+                        slot = (kc + i) % kKS
+                        assert smem_a[slot] == [(u, kb + i)] * 4, (smem_a[slot], u, kb + i)
+                        assert smem_b[slot] == (u, kb + i), (smem_b[slot], u, kb + i)
+                        log["mma"].append((u, kb + i, d))
+                        inflight.append(lambda slot=slot: empty_k[slot].arrive())
+                    kb += nkb; kc += nkb
                 inflight.append(lambda d=d: dfull[d].arrive())
                 pc += 1
     def epi(w):
@@ -96,12 +105,13 @@ def sim(n_units, ng, kCS=3, kKS=4, D=4, SPAN=4, seed=0):
                 while not full_c[cs].done((cc // kCS) & 1): yield
                 assert smem_c[cs] == (u, st)
                 gcount = min(8, ng - 8 * st)
-                for j in range(gcount):
-                    ks = kc % kKS
-                    while not empty_k[ks].done(((kc // kKS) & 1) ^ 1): yield
-                    smem_a[ks] = (u, 8 * st + j)
+                j0 = (w // 4) if stage_parity else (w // 4) ^ (kc & 1)  # kernel: kj % 2 == w // 4
+                for j in range(j0, gcount, 2):
+                    kj = kc + j; ks = kj % kKS
+                    while not empty_k[ks].done(((kj // kKS) & 1) ^ 1): yield
+                    smem_a[ks][w % 4] = (u, 8 * st + j)
                     full_a[ks].arrive()
-                    kc += 1
+                kc += gcount
                 empty_c[cs].arrive()
                 cc += 1
     roles = [producer_codes(), producer_b(), mma()] + [epi(i) for i in range(4)] + [deq(i) for i in range(8)]
@@ -127,3 +137,18 @@ def test_protocol_completes_and_never_overwrites_live_slots(n_units, ng):
     for seed in range(3):
         ok, _ = sim(n_units, ng, seed=seed)
         assert ok, (n_units, ng, seed)
+
+
+def test_model_catches_stage_relative_parity_with_odd_group_counts():
+    # Splitting each stage's K-blocks by their index inside the stage lets one
+    # warp of a quarter run a whole ring lap ahead when a unit has an odd
+    # number of groups, so a slot parity aliases; the model must see it.
+    bad = 0
+    for ng in (5, 9, 17):
+        for seed in range(6):
+            try:
+                ok, _ = sim(7, ng, seed=seed, stage_parity=True)
+            except AssertionError:
+                ok = False
+            bad += not ok
+    assert bad > 0
