@@ -9,18 +9,22 @@
 //   after gate/up k down rows of routed expert k (once its gate/up rows landed)
 // Grid-wide data dependencies go through the workspace: every published word
 // carries the launch's epoch in its upper half (a reader sees either the old
-// word or the new one, never a mix), and one relaxed counter per exchange
-// (logits; activations) tells a reader when every block has published.
+// word or the new one, never a mix, and polls a word again until its epoch is
+// this launch's).  The logits are polled directly; for the activations, which
+// every block reads in full, one relaxed counter tells a reader when every
+// block has published, and late words are polled again after it.
 // Phases of a block:
 //   h -> limbs of h*gamma (the RMS factor r multiplies each gate/up dot
 //        product, so quantisation does not wait for the norm); r from a block sum
 //   router rows -> published logits
 //   shared expert gate/up (all warps)
-//   warp 0: wait for every block's logits; top-K (every block, same result);
+//   warp 0: poll every block's logits (16 words per lane in flight); top-K
+//           (every block, same result);
 //           issue the routed gate/up copies; softmax over the chosen
 //   routed gate/up rows expert by expert as their copies land
 //   SwiGLU of every expert's rows, times its routing weight -> published
-//   wait for every block's activations; one bulk copy; limbs of each 64-group
+//   wait for the activation counter; every thread loads its 12 words straight
+//   from the workspace (late ones polled together); limbs of each 64-group
 //   down rows of every expert as one long dot product per row -> h[rows] += y
 // Routing never leaves the device.  Every wait is bounded (1 s): on timeout the
 // block records MOE_ERR_TIMEOUT, waits (bounded) for its own copies in flight,
@@ -204,16 +208,13 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   const size_t gu_slot = a.plan.gu_slot, dn_slot = a.plan.dn_slot;
   const int part_stride = a.plan.part_stride;
   // mbarriers: [0] router rows, [1 + p] gate/up of expert p, [1 + NE + p] down
-  // of expert p (expert p = 0 is the shared expert when present), then h and
-  // the published activations
-  const int bar_h = 1 + 2 * NE, bar_a = bar_h + 1, nbar = bar_h + 2;
+  // of expert p (expert p = 0 is the shared expert when present), then h
+  const int bar_h = 1 + 2 * NE, nbar = bar_h + 1;
   float* const hbuf = reinterpret_cast<float*>(G + a.plan.off_hbuf);
-  const unsigned long long* const abuf = reinterpret_cast<const unsigned long long*>(G + a.plan.off_abuf);
 
   // ---- prologue.
-  // Every block reads all of h, the logits and the activations; each comes in
-  // as one bulk copy per block (a few large requests), not as per-thread loads
-  // of the same lines by every block.
+  // Every block reads all of h (one bulk copy), the logits and the
+  // activations (polled words).
   // Barrier set-up, visible to every thread and to the copy engine before the
   // first copy is issued:
   if (tid == 0) {
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         named_sync(1, kBlock);
         if (lane == 0) STAMP(5);
         bool ok = true;
-        bool ready = lane != 0 || wait_count(a.hdr, &a.hdr->published_logits, (unsigned long long)P * expect);
+        bool ready = true;  // the words carry their epoch: polled directly
         if (lane == 0) STAMP(6);
         ready = __all_sync(0xffffffffu, ready);
         uint32_t key[32];
@@ -443,15 +444,15 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         // its words in flight together; a word not yet visible is polled again)
         const int mine = E > lane ? (E - lane + 31) / 32 : 0;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          if (ch * 8 < mine && ready) {  // lane-dependent, no collectives inside
-            float v[8];
-            ready = poll_pub<8>(a.hdr, a.pub_logits + lane + 256 * ch, 32, min(8, mine - ch * 8), expect, v);
+        for (int ch = 0; ch < 2; ++ch) {
+          if (ch * 16 < mine && ready) {  // lane-dependent, no collectives inside
+            float v[16];
+            ready = poll_pub<16>(a.hdr, a.pub_logits + lane + 512 * ch, 32, min(16, mine - ch * 16), expect, v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (ch * 8 + i < mine) {
+            for (int i = 0; i < 16; ++i) {
+              if (ch * 16 + i < mine) {
                 ok &= isfinite(v[i]);
-                key[ch * 8 + i] = fkey(v[i]);
+                key[ch * 16 + i] = fkey(v[i]);
               }
             }
           }
@@ -550,24 +551,17 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       red_relaxed_add_u64(&a.hdr->published_act, 1ull);
       s_mask[4] |= 2u;
     }
-    // activation reader: one thread waits on the counter and copies every
-    // published activation into this block's gate/up area (its generic reads
-    // are complete: block barrier above), then every thread checks the epochs
-    // of the words it needs and polls a late word again
+    // activation reader: one thread waits on the counter, then every thread
+    // loads the words it needs and polls the late ones again.  (Polling the
+    // words without the counter, as for the logits, cost 3.7 us a token on
+    // B300: 148 blocks re-reading 40 KB each while others still compute.)
     if (tid == 0) {
       STAMP(17);
       const bool ok = wait_count(a.hdr, &a.hdr->published_act, (unsigned long long)P * expect);
       STAMP(18);
-      if (ok) {
-        fence_proxy_async();
-        mbar_expect_tx(&bar[bar_a], (uint32_t)a.plan.abuf_bytes);
-        bulk_g2s(G + a.plan.off_abuf, a.pub_act, (uint32_t)a.plan.abuf_bytes, &bar[bar_a]);
-        s_mask[0] |= 1u << bar_a;
-      }
       s_mask[5] = ok ? 0u : 1u;
     }
     if (__syncthreads_or(tid == 0 && s_mask[5] != 0u)) goto cleanup;
-    warp_wait(bar_a);
     if (tid == 0) STAMP(19);
 
     // ---- limbs of every weighted a: a half-warp per group, 2 groups per warp
@@ -583,6 +577,9 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         uint8_t* vs[kActPasses];
         float2* es[kActPasses];
         float one[kActPasses];
+        size_t w0s[kActPasses];
+        unsigned long long wv[kActPasses][4];
+        bool late = false;
 #pragma unroll
         for (int k = 0; k < kActPasses; ++k) {
           const int gi = base0 + 2 * kWarps * k + (lane >> 4);
@@ -594,18 +591,44 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
           es[k] = AE + (size_t)p * ngi + g;
           one[k] = 1.0f;
           // values 4j .. 4j+3 of the group sit at slots j, j + 16, j + 32, j + 48
-          const size_t w0 = (size_t)p * I + g * kGroup + (lane & 15);
-          float v[4];
-          bool late = false;
+          w0s[k] = (size_t)p * I + g * kGroup + (lane & 15);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const unsigned long long w = abuf[w0 + 16 * i];
-            late |= !pub_ready(w, expect);
-            v[i] = pub_value(w);
+            wv[k][i] = ld_pub(a.pub_act + w0s[k] + 16 * i);
+            late |= !pub_ready(wv[k][i], expect);
           }
-          if (late && ready) ready = poll_pub<4>(a.hdr, a.pub_act + w0, 16, 4, expect, v);
-          xs[k] = make_float4(v[0], v[1], v[2], v[3]);
         }
+        // words that were not yet visible when the copy ran: polled again, all
+        // of this thread's together
+        if (late && ready) {
+          const unsigned long long t0 = globaltimer();
+          int spins = 0;
+          while (late) {
+            late = false;
+#pragma unroll
+            for (int k = 0; k < kActPasses; ++k)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (!pub_ready(wv[k][i], expect)) wv[k][i] = ld_pub(a.pub_act + w0s[k] + 16 * i);
+#pragma unroll
+            for (int k = 0; k < kActPasses; ++k)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) late |= !pub_ready(wv[k][i], expect);
+            if (late && (++spins & 63) == 0) {
+              if (*(volatile uint32_t*)&a.hdr->abort || globaltimer() - t0 > kTimeoutNs) {
+                if (globaltimer() - t0 > kTimeoutNs) {
+                  atomicOr(&a.hdr->status, ST_TIMEOUT);
+                  atomicExch(&a.hdr->abort, 1u);
+                }
+                ready = false;
+                break;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kActPasses; ++k)
+          xs[k] = make_float4(pub_value(wv[k][0]), pub_value(wv[k][1]), pub_value(wv[k][2]), pub_value(wv[k][3]));
         fin &= quantize_groups<kActPasses>(xs, lane, st, vs, ngi, gs, es, one);
       }
       if (!ready) atomicOr(&s_mask[1], 1u);
@@ -727,11 +750,9 @@ bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, i
   p.off_sgu = sub(has_shared ? (size_t)p.rows_gu * fs.gu_pair : 0);
   p.off_rt = sub((size_t)p.rows_r * H * 2);
   p.off_hbuf = sub((size_t)H * 4);  // h, one bulk copy
-  // after the gate/up phase: down partials, then the published activations
-  p.abuf_bytes = (size_t)NE * I * 8;
+  // after the gate/up phase: the down partials
   const size_t post = ((size_t)p.rows_d * NE * fr.ng_i * 4 + 127) / 128 * 128;
-  p.off_abuf = post;
-  p.off_g = take(std::max(std::max(pre, (size_t)K * p.gu_slot), post + p.abuf_bytes));
+  p.off_g = take(std::max(std::max(pre, (size_t)K * p.gu_slot), post));
   // limbs: of x first (read into registers), later of every expert's activation
   const size_t ngroups = std::max((size_t)NE * fr.ng_i, (size_t)fr.ng_h);
   p.off_al = take(ngroups * kLimbBytes);
@@ -740,7 +761,7 @@ bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, i
   p.off_part = take((size_t)NE * p.part_stride * 4);
   p.off_rpart = take((size_t)p.rows_r * kWarps * 4);
   p.off_y = take((size_t)p.rows_d * 4);
-  p.off_bar = take((size_t)(1 + 2 * NE + 2) * 8);
+  p.off_bar = take((size_t)(1 + 2 * NE + 1) * 8);
   p.off_misc = take(256);
   p.total = o + 128;  // slack for rounding the dynamic base up to 128 bytes
   if (p.total > (size_t)optin) return false;

@@ -122,8 +122,6 @@ struct DecodePlan {
   size_t off_dn;    // down slices, slot p at off_dn + p * dn_slot
   size_t off_g;     // gate/up area (before routing: shared slice, router rows)
   size_t off_sgu, off_rt, off_hbuf;  // relative to off_g, before routing
-  size_t off_abuf;    // relative to off_g, after the gate/up phase (down partials at 0)
-  size_t abuf_bytes;  // bulk copy of the published activations
   size_t off_al, off_ae;   // limbs of x, later of every expert's activation
   size_t off_part, off_rpart, off_y, off_bar, off_misc;
   size_t total;

@@ -266,7 +266,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   const int nrows = a.E + (a.has_gate ? 1 : 0);
   for (int e = tid; e < nrows; e += blockDim.x) {
     float v = part[e];
-    for (int sp = 1; sp < a.splits; ++sp) v += part[sp * pstride + e];
+    int sp = 1;
+    for (; sp + 8 <= a.splits; sp += 8) {  // eight loads in flight, added in split order
+      float p[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p[i] = part[(size_t)(sp + i) * pstride + e];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v += p[i];
+    }
+    for (; sp < a.splits; ++sp) v += part[(size_t)sp * pstride + e];
     if (e < a.E && a.offset) v += a.offset[(size_t)b * a.E + e];
     s_lg[e] = v;
   }
@@ -322,28 +330,42 @@ __global__ void __launch_bounds__(kBlock) bucket_kernel(BucketArgs a) {
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&cnt[ids[i]], 1);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int u = 0, base = 0;
-    if (a.has_shared) {
-      for (int b0 = 0; b0 < a.B; b0 += kSharedChunk) {
-        a.uniq_e[u] = -1;
-        a.uniq_off[u] = b0;
-        ++u;
-      }
-      base = a.B;
-    }
-    int run = base;
-    for (int e = 0; e < a.E; ++e) {
-      off[e] = run;
-      if (cnt[e] > 0) {
-        a.uniq_e[u] = e;
-        a.uniq_off[u] = run;
-        ++u;
-      }
-      run += cnt[e];
-    }
-    a.uniq_off[u] = run;
-    *a.n_uniq = u;
+  // thread t owns experts 2t and 2t + 1: one block-wide exclusive scan of
+  // (entries, touched experts) in expert order gives every expert's first
+  // entry and its work-item number
+  __shared__ int s_wsum[2][kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int e0 = 2 * tid, e1 = 2 * tid + 1;
+  const int c0 = e0 < a.E ? cnt[e0] : 0, c1 = e1 < a.E ? cnt[e1] : 0;
+  const int f0 = c0 > 0, f1 = c1 > 0;
+  int ic = c0 + c1, iu = f0 + f1;  // inclusive scans within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int vc = __shfl_up_sync(0xffffffffu, ic, o), vu = __shfl_up_sync(0xffffffffu, iu, o);
+    if (lane >= o) { ic += vc; iu += vu; }
+  }
+  if (lane == 31) { s_wsum[0][wid] = ic; s_wsum[1][wid] = iu; }
+  __syncthreads();
+  int wc = 0, wu = 0;  // totals of the earlier warps
+  for (int w = 0; w < wid; ++w) { wc += s_wsum[0][w]; wu += s_wsum[1][w]; }
+  const int n_shared_items = a.has_shared ? (a.B + kSharedChunk - 1) / kSharedChunk : 0;
+  const int base = a.has_shared ? a.B : 0;  // the shared expert's entries come first
+  const int xc = base + wc + ic - (c0 + c1), xu = n_shared_items + wu + iu - (f0 + f1);
+  if (e0 < a.E) {
+    off[e0] = xc;
+    if (f0) { a.uniq_e[xu] = e0; a.uniq_off[xu] = xc; }
+  }
+  if (e1 < a.E) {
+    off[e1] = xc + c0;
+    if (f1) { a.uniq_e[xu + f0] = e1; a.uniq_off[xu + f0] = xc + c0; }
+  }
+  if (tid < n_shared_items) {
+    a.uniq_e[tid] = -1;
+    a.uniq_off[tid] = tid * kSharedChunk;
+  }
+  if (tid == blockDim.x - 1) {  // the last thread's inclusive totals are the block's
+    a.uniq_off[xu + f0 + f1] = xc + c0 + c1;
+    *a.n_uniq = xu + f0 + f1;
   }
   __syncthreads();
   // entry i = (b, k): its position among entries of the same expert is the
@@ -638,7 +660,7 @@ cudaError_t launch_topk(const TopkArgs& a, int B, cudaStream_t s) {
 }
 cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t s) {
   const size_t sm = (size_t)(2 * a.E + a.B * a.K) * sizeof(int);
-  if (sm > 48 * 1024) return cudaErrorInvalidValue;
+  if (sm > 48 * 1024 || a.E > 2 * kBlock) return cudaErrorInvalidValue;  // two experts per thread
   bucket_kernel<<<1, kBlock, sm, s>>>(a);
   return cudaGetLastError();
 }

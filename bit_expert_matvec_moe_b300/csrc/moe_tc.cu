@@ -194,16 +194,6 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 // Bounded mbarrier wait that also gives up once another role of the CTA has.
-// A phase that has already completed is seen by test_wait (non-blocking, a few
-// tens of cycles); try_wait, which may suspend the thread, only after that.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile("{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-               : "=r"(ok)
-               : "r"(su32(bar)), "r"(parity)
-               : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort) {
   if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();

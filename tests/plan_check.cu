@@ -46,7 +46,7 @@ bool check(int nsm, int optin, int H, int I, int E, int K, int bits, int sbits, 
       {"gate/up partials", p.off_part, p.off_part + (size_t)NE * p.part_stride * 4},
       {"router partials", p.off_rpart, p.off_rpart + (size_t)p.rows_r * moe::kWarps * 4},
       {"down sums", p.off_y, p.off_y + (size_t)p.rows_d * 4},
-      {"mbarriers", p.off_bar, p.off_bar + (size_t)(1 + 2 * NE + 2) * 8},
+      {"mbarriers", p.off_bar, p.off_bar + (size_t)(1 + 2 * NE + 1) * 8},
       {"misc", p.off_misc, p.off_misc + 192}};
   for (size_t i = 0; i < rs.size(); ++i) {
     if (rs[i].at % 128) return fail(rs[i].name);
@@ -58,9 +58,8 @@ bool check(int nsm, int optin, int H, int I, int E, int K, int bits, int sbits, 
   if (pre_end > gsz) return fail("pre-routing pieces outside the gate/up area");
   if ((size_t)K * p.gu_slot > gsz) return fail("routed slices outside the gate/up area");
   const size_t pdn = (size_t)p.rows_d * NE * ngi * 4;
-  if (p.off_abuf < pdn || p.off_abuf + p.abuf_bytes > gsz || p.abuf_bytes != (size_t)NE * I * 8)
-    return fail("down partials / activation copy outside the gate/up area");
-  if (p.off_sgu % 16 || p.off_rt % 16 || p.off_hbuf % 16 || p.off_abuf % 16 || p.gu_slot % 16 || p.dn_slot % 16)
+  if (pdn > gsz) return fail("down partials outside the gate/up area");
+  if (p.off_sgu % 16 || p.off_rt % 16 || p.off_hbuf % 16 || p.gu_slot % 16 || p.dn_slot % 16)
     return fail("copy destination not 16-byte aligned");
   if (p.total > (size_t)optin) return fail("plan larger than the opt-in shared memory");
   for (int c = 0; c < p.P; ++c) {
