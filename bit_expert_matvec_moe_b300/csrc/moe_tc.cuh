@@ -25,10 +25,13 @@
 // low bits at every MMA step (measured on B300: summed over all 4096 inputs of
 // a gate/up row in one accumulator, the expert output errs by ~2e-3 by the
 // tests' relative-error measure, the bar itself).  So each accumulator spans
-// only kSpanKB K-blocks (256 inputs); the epilogue adds the partial sums in
-// fp32 registers.  A host model of the truncating accumulation reproduces the
-// hardware error and puts this split at ~2e-4; bf16 weights (8 bits) would not
-// meet 2e-3 even with exact sums.
+// only kSpanKB K-blocks (512 inputs); the epilogue adds the partial sums in
+// fp32 registers.  Measured on B300 over 64 skewed-routing tokens of the
+// full-width layer (max relative error of y / of y - h): spans of 256 inputs
+// 4.7e-4 / 2.7e-4, 512 inputs 4.9e-4 / 6.6e-4, 1024 inputs 9.9e-4 / 1.1e-3;
+// each doubling saves 8 % / 2 % of the batch-128 layer call (fewer span
+// boundaries in the MMA loop), so 512 keeps a 3x margin under the bar.  bf16
+// weights (8 bits) would not meet 2e-3 even with exact sums.
 //
 // Operand layouts (shared memory, K-major, 128-byte swizzle)
 // ----------------------------------------------------------
@@ -63,7 +66,7 @@ constexpr int kTcTok = 32;           // tokens per unit at most (MMA N = 2 * tok
 constexpr int kStageGroups = 8;      // groups per code stage (one TMA box = 128 bytes of codes per row)
 constexpr int kCodeSlots = 3;        // code stages in flight
 constexpr int kKSlots = 8;           // K-blocks in flight (A in tensor memory, B in shared memory)
-constexpr int kSpanKB = 4;           // K-blocks summed in one accumulator before the epilogue takes it
+constexpr int kSpanKB = 8;           // K-blocks summed in one accumulator before the epilogue takes it
 constexpr int kDBufs = 4;            // accumulators in tensor memory (a ring of partial sums)
 constexpr int kDCols = 64;           // tensor-memory columns per accumulator (N <= 64)
 constexpr int kTmemACol0 = kDBufs * kDCols;  // A operand: one 32-column block (64 fp16 per lane) per K slot

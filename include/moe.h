@@ -60,7 +60,7 @@ typedef enum {
                                  (instead of a cooperative launch; see moe_layer_decode) */
 #define MOE_TENSOR_CORES 16   /* moe_layer_decode and moe_expert_forward, B > 1: expert matvecs as
                                  tensor-core contractions (tcgen05, fp16 dequantised weights x fp16
-                                 hi/lo activations, partial sums of 256 inputs added in fp32).
+                                 hi/lo activations, partial sums of 512 inputs added in fp32).
                                  Workspace sizes include the path's operand buffers when the flag
                                  is set; moe_workspace_bytes must be given the same flags. */
 

@@ -2,7 +2,7 @@
 (bit_expert_matvec_moe_b300/csrc/moe_tc.cu, tc_contract_kernel): the warp
 roles are modelled as coroutines with the kernel's loop structure and its
 slot / parity arithmetic (code ring of 3, K-block ring of 8, a ring of 4
-accumulators each holding the partial sum of up to 4 K-blocks; the MMA warp
+accumulators each holding the partial sum of up to 8 K-blocks; the MMA warp
 takes K-blocks in pairs; the two dequantising warps of each tensor-memory lane
 quarter take the even and the odd K-blocks, counted over the whole launch so
 that every K slot has one writer per quarter), barriers with the PTX
@@ -31,7 +31,7 @@ class Bar:
     def done(s, parity):  # try_wait.parity semantics
         return (s.phase & 1) != parity
 
-def sim(n_units, ng, kCS=3, kKS=8, D=4, SPAN=4, PAIR=2, seed=0, stage_parity=False):
+def sim(n_units, ng, kCS=3, kKS=8, D=4, SPAN=8, PAIR=2, seed=0, stage_parity=False):
     rnd = random.Random(seed)
     nst = (ng + 7) // 8
     full_c = [Bar(1) for _ in range(kCS)]; empty_c = [Bar(8) for _ in range(kCS)]
@@ -135,8 +135,9 @@ def sim(n_units, ng, kCS=3, kKS=8, D=4, SPAN=4, PAIR=2, seed=0, stage_parity=Fal
 @pytest.mark.parametrize("ng", [1, 2, 5, 8, 9, 16, 17, 64])
 def test_protocol_completes_and_never_overwrites_live_slots(n_units, ng):
     for seed in range(3):
-        ok, _ = sim(n_units, ng, seed=seed)
-        assert ok, (n_units, ng, seed)
+        for span in (4, 8):
+            ok, _ = sim(n_units, ng, SPAN=span, seed=seed)
+            assert ok, (n_units, ng, span, seed)
 
 
 def test_model_catches_stage_relative_parity_with_odd_group_counts():
