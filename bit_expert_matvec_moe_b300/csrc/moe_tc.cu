@@ -227,9 +227,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
   uint64_t* full_c = bars;                   // code stage landed (TMA bytes)
   uint64_t* empty_c = full_c + kCodeSlots;   // code stage read by the 8 dequantising warps
-  uint64_t* full_a = empty_c + kCodeSlots;   // A K-block written by the 8 dequantising warps
-  uint64_t* full_b = full_a + kKSlots;       // B K-block landed (TMA bytes)
-  uint64_t* empty_k = full_b + kKSlots;      // K-block read by the MMAs (commit)
+  // K slot ready: the 4 dequantising warps of its parity have written A and
+  // the B copy has landed (the B producer's expect_tx is the fifth arrival)
+  uint64_t* full_a = empty_c + kCodeSlots;
+  uint64_t* empty_k = full_a + kKSlots;      // K-block read by the MMAs (commit)
   uint64_t* dfull = empty_k + kKSlots;       // partial sum complete (commit)
   uint64_t* dempty = dfull + kDBufs;         // partial sum read by the 4 epilogue warps
   uint64_t* drain = dempty + kDBufs;
@@ -243,8 +244,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&empty_c[i], 8);
     }
     for (int i = 0; i < kKSlots; ++i) {
-      mbar_init(&full_a[i], 4);
-      mbar_init(&full_b[i], 1);
+      mbar_init(&full_a[i], 5);
       mbar_init(&empty_k[i], 1);
     }
     for (int i = 0; i < kDBufs; ++i) {
@@ -316,12 +316,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t slot = kc % kKSlots;
           if (!(ok = tc_wait(&empty_k[slot], ((kc / kKSlots) & 1u) ^ 1u, abort))) break;
           uint8_t* dst = sm + kOffK + slot * kKSlotBytes;
-          mbar_expect_tx(&full_b[slot], (uint32_t)boxes * kBBoxBytes);
+          mbar_expect_tx(&full_a[slot], (uint32_t)boxes * kBBoxBytes);
           for (int i = 0; i < boxes; ++i)
-            tma_load_2d(dst + i * kBBoxBytes, &m_b, kb * 64, 2 * ch.e0 + (int)kBBoxRows * i, &full_b[slot]);
+            tma_load_2d(dst + i * kBBoxBytes, &m_b, kb * 64, 2 * ch.e0 + (int)kBBoxRows * i, &full_a[slot]);
         }
       }
-      drain_ring(full_b, kKSlots, kc);
+      // (the slots' phases also wait for the dequantising warps; after a give-up
+      // the bounded wait then just outlasts the copies in flight)
+      drain_ring(full_a, kKSlots, kc);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) {
             for (int i = 0; i < nkb && w; ++i) {
               const uint32_t sl = (kc + i) % kKSlots, pa = ((kc + i) / kKSlots) & 1u;
-              w = tc_wait(&full_a[sl], pa, abort) && tc_wait(&full_b[sl], pa, abort);
+              w = tc_wait(&full_a[sl], pa, abort);
             }
           }
           if (!(ok = __all_sync(0xffffffffu, w))) break;

@@ -95,7 +95,7 @@ constexpr int kTcThreads = kTcWarps * 32;
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffCodes = kOffK + kKSlots * kKSlotBytes;
 constexpr uint32_t kOffBars = kOffCodes + kCodeSlots * kCodeSlotBytes;
-constexpr int kNumBars = 2 * kCodeSlots + 3 * kKSlots + 2 * kDBufs + 1;
+constexpr int kNumBars = 2 * kCodeSlots + 2 * kKSlots + 2 * kDBufs + 1;
 constexpr uint32_t kOffMisc = kOffBars + 8 * kNumBars;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base

@@ -5,7 +5,8 @@ slot / parity arithmetic (code ring of 3, K-block ring of 8, a ring of 4
 accumulators each holding the partial sum of up to 8 K-blocks; the MMA warp
 takes K-blocks in pairs; the two dequantising warps of each tensor-memory lane
 quarter take the even and the odd K-blocks, counted over the whole launch so
-that every K slot has one writer per quarter), barriers with the PTX
+that every K slot has one writer per quarter; a K slot's barrier counts the
+four A writers and the B producer, whose copy lands on it), barriers with the PTX
 test_wait / try_wait.parity semantics and the kernel's arrival counts, and TMA
 landings and MMA commits completing in random order.  Every configuration
 must finish without a stuck wait, every MMA must find the A and B blocks of
@@ -35,7 +36,8 @@ def sim(n_units, ng, kCS=3, kKS=8, D=4, SPAN=8, PAIR=2, seed=0, stage_parity=Fal
     rnd = random.Random(seed)
     nst = (ng + 7) // 8
     full_c = [Bar(1) for _ in range(kCS)]; empty_c = [Bar(8) for _ in range(kCS)]
-    full_a = [Bar(4) for _ in range(kKS)]; full_b = [Bar(1) for _ in range(kKS)]; empty_k = [Bar(1) for _ in range(kKS)]
+    # full_a: 4 dequantising warps + the B producer's expect_tx (B's bytes land on the same barrier)
+    full_a = [Bar(5) for _ in range(kKS)]; empty_k = [Bar(1) for _ in range(kKS)]
     dfull = [Bar(1) for _ in range(D)]; dempty = [Bar(4) for _ in range(D)]
     smem_c = [None]*kCS; smem_a = [[None]*4 for _ in range(kKS)]; smem_b = [None]*kKS; tmem = [None]*D
     inflight = []  # (callback) async completions (TMA, MMA commit)
@@ -58,10 +60,10 @@ def sim(n_units, ng, kCS=3, kKS=8, D=4, SPAN=8, PAIR=2, seed=0, stage_parity=Fal
             for kb in range(ng):
                 slot = kc % kKS
                 while not empty_k[slot].done(((kc // kKS) & 1) ^ 1): yield
-                full_b[slot].expect_tx(7)
+                full_a[slot].expect_tx(7)
                 tag = (u, kb)
                 def land(slot=slot, tag=tag):
-                    smem_b[slot] = tag; full_b[slot].complete_tx(7)
+                    smem_b[slot] = tag; full_a[slot].complete_tx(7)
                 inflight.append(land)
                 kc += 1
     def mma():
@@ -77,7 +79,7 @@ def sim(n_units, ng, kCS=3, kKS=8, D=4, SPAN=8, PAIR=2, seed=0, stage_parity=Fal
                     nkb = min(PAIR, kb1 - kb)
                     for i in range(nkb):
                         slot = (kc + i) % kKS; par = ((kc + i) // kKS) & 1
-                        while not (full_a[slot].done(par) and full_b[slot].done(par)): yield
+                        while not full_a[slot].done(par): yield
                     for i in range(nkb):
                         slot = (kc + i) % kKS
                         assert smem_a[slot] == [(u, kb + i)] * 4, (smem_a[slot], u, kb + i)
