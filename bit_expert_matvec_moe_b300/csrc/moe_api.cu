@@ -250,6 +250,7 @@ moe_status moe_route(const moe_dims* dims, const float* xn, int32_t B, const uin
   const WsLayout L = ws_layout(*dims, B);
   if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PdlScope pdl_scope((dims->flags & MOE_PDL) != 0);
   RouterArgs r{};
   r.xn = xn;
   r.B = B;
@@ -288,6 +289,7 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   const WsLayout L = ws_layout(*dims, B);
   if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PdlScope pdl_scope((dims->flags & MOE_PDL) != 0);
   const int H = dims->hidden, I = dims->inter;
   WsHeader* hdr = at<WsHeader>(ws, 0);
   if (tc_refused(*dims, B)) return MOE_ERR_UNSUPPORTED;
@@ -443,7 +445,8 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
     }
   }
 
-  // multi-kernel path
+  // multi-kernel path (its kernels chained by programmatic launch with MOE_PDL)
+  PdlScope pdl_scope((d.flags & MOE_PDL) != 0);
   const int K = d.top_k, E = d.n_experts, H = d.hidden, I = d.inter;
   const int nslots = K + has_shared;
   NormQuantArgs nq{};

@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <string>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "moe_device.cuh"
@@ -164,6 +165,36 @@ bool decode_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_
 bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, int shared_bits, int has_shared,
                      int has_gate, DecodePlan* out);
 cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s);
+
+// Launches of the multi-kernel path.  Inside a PdlScope that is on, kernels go
+// out with programmatic stream serialisation: each may be scheduled while its
+// predecessor on the stream drains, and every such kernel starts with
+// griddepcontrol.wait (pdl_wait_prior) before it touches memory, so the
+// ordering of the stream is kept; the gain is the launch latency between the
+// short kernels of a batched call.
+extern thread_local bool t_launch_pdl;
+struct PdlScope {
+  bool prev;
+  explicit PdlScope(bool on) : prev(t_launch_pdl) { t_launch_pdl = on; }
+  ~PdlScope() { t_launch_pdl = prev; }
+};
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (t_launch_pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Text returned by moe_last_error_message() for this thread.
 void set_last_error(const std::string& msg);

@@ -5,6 +5,8 @@
 
 namespace moe {
 
+thread_local bool t_launch_pdl = false;  // see PdlScope
+
 // ---------------------------------------------------------------------------
 // moe_pack_weights: canonical (codes, scales, biases) x 3 -> one blob
 // ---------------------------------------------------------------------------
@@ -73,6 +75,8 @@ __global__ void pack_kernel(PackArgs a) {
 // is written to xn_out; the limbs of (do_norm ? xn : in) go to q (row b at
 // q + b * ng * 128 bytes) and the group factors to e.
 __global__ void __launch_bounds__(kBlock) norm_quant_kernel(NormQuantArgs a) {
+  pdl_wait_prior();  // no-op unless launched with programmatic serialisation
+  pdl_launch_dependents();
   extern __shared__ float4 nq_smem[];
   float* v = reinterpret_cast<float*>(nq_smem);
   __shared__ float red[kBlock / 32];
@@ -153,6 +157,8 @@ __device__ __forceinline__ void load_vec(const float* p, float (&v)[N]) {
 
 template <int RT, int TT, int TX>
 __global__ void __launch_bounds__(kRtThreads) router_kernel(RouterArgs a) {
+  pdl_wait_prior();  // no-op unless launched with programmatic serialisation
+  pdl_launch_dependents();
   constexpr int TR = kRtThreads / TX, TOK = TT * TX;
   static_assert(RT * TR == kRtRows, "router row tile");
   constexpr int WSTR = kRtRows + 4, XSTR = TOK + 4;  // k-major strides (16-byte multiples)
@@ -257,6 +263,8 @@ __global__ void __launch_bounds__(kRtThreads) router_kernel(RouterArgs a) {
 constexpr int kTopkPer = 32;  // experts per lane: up to 1024 experts
 constexpr int kTopkThreads = 256;
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
+  pdl_wait_prior();  // no-op unless launched with programmatic serialisation
+  pdl_launch_dependents();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   // logits of this token: the router's split partial sums added in split order,
   // then the caller's offset (routed experts only)
@@ -320,6 +328,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
 // [uniq_off[u], uniq_off[u + 1]); expert id -1 is the shared expert.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kBlock) bucket_kernel(BucketArgs a) {
+  pdl_wait_prior();  // no-op unless launched with programmatic serialisation
+  pdl_launch_dependents();
   extern __shared__ int bk_smem[];
   const int n = a.B * a.K;
   int* cnt = bk_smem;     // [E]
@@ -519,6 +529,8 @@ __device__ void gateup_tile(const GateUpArgs& a, const uint8_t* blob, const Fmt&
 }
 
 __global__ void __launch_bounds__(kWsThreads, 2) gateup_kernel(GateUpArgs a) {
+  pdl_wait_prior();  // no-op unless launched with programmatic serialisation
+  pdl_launch_dependents();
   extern __shared__ __align__(16) uint8_t sm[];
   int item = blockIdx.y;
   const uint8_t* blob;
@@ -571,6 +583,8 @@ __device__ void down_tile(const DownArgs& a, const uint8_t* blob, const Fmt& f, 
 }
 
 __global__ void __launch_bounds__(kWsThreads, 2) down_kernel(DownArgs a) {
+  pdl_wait_prior();  // no-op unless launched with programmatic serialisation
+  pdl_launch_dependents();
   extern __shared__ __align__(16) uint8_t sm[];
   int item = blockIdx.y;
   const uint8_t* blob;
@@ -601,6 +615,8 @@ __global__ void __launch_bounds__(kWsThreads, 2) down_kernel(DownArgs a) {
 // the single-expert output out[b] = (acc ? out[b] : 0) + row_w[b] d[b][0]
 // ---------------------------------------------------------------------------
 __global__ void combine_kernel(CombineArgs a) {
+  pdl_wait_prior();  // no-op unless launched with programmatic serialisation
+  pdl_launch_dependents();
   const size_t n = (size_t)a.B * a.H;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
     const int b = (int)(i / a.H), j = (int)(i % a.H);
@@ -633,8 +649,7 @@ cudaError_t launch_norm_quant(const NormQuantArgs& a, int B, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(norm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
   }
-  norm_quant_kernel<<<B, kBlock, sm, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(norm_quant_kernel, dim3(B), dim3(kBlock), sm, s, a);
 }
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   const int rows = a.E + (a.gate ? 1 : 0);
@@ -643,26 +658,23 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   if (a.stages_per_split < 1 || splits != router_splits(a.B, a.H, a.E)) return cudaErrorInvalidValue;
   dim3 grid((rows + kRtRows - 1) / kRtRows, (a.B + tok - 1) / tok, splits);
   if (tok == 16)
-    router_kernel<2, 2, 8><<<grid, kRtThreads, 0, s>>>(a);
+    return launch_kernel(router_kernel<2, 2, 8>, grid, dim3(kRtThreads), 0, s, a);
   else if (tok == 32)
-    router_kernel<4, 2, 16><<<grid, kRtThreads, 0, s>>>(a);
+    return launch_kernel(router_kernel<4, 2, 16>, grid, dim3(kRtThreads), 0, s, a);
   else
-    router_kernel<4, 4, 16><<<grid, kRtThreads, 0, s>>>(a);
-  return cudaGetLastError();
+    return launch_kernel(router_kernel<4, 4, 16>, grid, dim3(kRtThreads), 0, s, a);
 }
 int router_stages_per_split(int B, int H, int E) {
   const int stages = H / kRtK, sp = router_splits(B, H, E);
   return (stages + sp - 1) / sp;
 }
 cudaError_t launch_topk(const TopkArgs& a, int B, cudaStream_t s) {
-  topk_kernel<<<B, kTopkThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(topk_kernel, dim3(B), dim3(kTopkThreads), 0, s, a);
 }
 cudaError_t launch_bucket(const BucketArgs& a, cudaStream_t s) {
   const size_t sm = (size_t)(2 * a.E + a.B * a.K) * sizeof(int);
   if (sm > 48 * 1024 || a.E > 2 * kBlock) return cudaErrorInvalidValue;  // two experts per thread
-  bucket_kernel<<<1, kBlock, sm, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(bucket_kernel, dim3(1), dim3(kBlock), sm, s, a);
 }
 // shared memory of one weight-stationary tile: staged rows and the partials of
 // one token chunk ([kTok][rows][row chunks]); sized for the wider code width
@@ -677,8 +689,7 @@ cudaError_t launch_gateup(const GateUpArgs& a, int items, cudaStream_t s) {
   const cudaError_t e = ensure_dynamic_smem(gateup_kernel, (int)sm, configured);
   if (e != cudaSuccess) return e;
   dim3 grid((a.I + tile / 2 - 1) / (tile / 2), items);
-  gateup_kernel<<<grid, kWsThreads, sm, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(gateup_kernel, grid, dim3(kWsThreads), sm, s, a);
 }
 cudaError_t launch_down(const DownArgs& a, int items, cudaStream_t s) {
   const int tile = dn_tile_rows(a.I);
@@ -688,14 +699,12 @@ cudaError_t launch_down(const DownArgs& a, int items, cudaStream_t s) {
   const cudaError_t e = ensure_dynamic_smem(down_kernel, (int)sm, configured);
   if (e != cudaSuccess) return e;
   dim3 grid((a.H + tile - 1) / tile, items);
-  down_kernel<<<grid, kWsThreads, sm, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(down_kernel, grid, dim3(kWsThreads), sm, s, a);
 }
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   const size_t n = (size_t)a.B * a.H;
   const int grid = (int)std::min<size_t>((n + 255) / 256, 148 * 8);
-  combine_kernel<<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, grid, dim3(256), 0, s, a);
 }
 
 }  // namespace moe

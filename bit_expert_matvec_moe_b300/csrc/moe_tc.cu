@@ -53,6 +53,8 @@ namespace tc {
 // work list: chunks of at most kTcTok entries per touched expert
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(32) tc_plan_kernel(TcPlanArgs a) {
+  pdl_wait_prior();  // no-op unless launched with programmatic serialisation
+  pdl_launch_dependents();
   const int lane = threadIdx.x;
   const int nu = *a.n_uniq;
   int total = 0;
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(32) tc_plan_kernel(TcPlanArgs a) {
 // Work list of one expert applied to tokens 0 .. B-1 (moe_expert_forward): a
 // single item, taken through the shared-expert tensor maps.
 __global__ void tc_single_item_kernel(int B, int* n_uniq, int* uniq_e, int* uniq_off, int* ent) {
+  pdl_wait_prior();
+  pdl_launch_dependents();
   for (int j = threadIdx.x; j < B; j += blockDim.x) ent[j] = j;
   if (threadIdx.x == 0) {
     *n_uniq = 1;
@@ -105,6 +109,8 @@ __global__ void tc_single_item_kernel(int B, int* n_uniq, int* uniq_e, int* uniq
 // B operand rows: fp16 hi / lo of each entry's activation, scaled per entry
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tc_pack_kernel(TcPackArgs a) {
+  pdl_wait_prior();
+  pdl_launch_dependents();
   const int j = blockIdx.x;
   const int total = a.uniq_off[*a.n_uniq];
   if (j >= total) return;
@@ -272,6 +278,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  // set-up above overlaps the previous kernel when launched with programmatic
+  // serialisation; nothing it wrote is read before this wait
+  pdl_wait_prior();
+  pdl_launch_dependents();
   const int n_units = *a.n_chunks * a.tiles;
   const int nst = (a.ng + kStageGroups - 1) / kStageGroups;
 
@@ -570,19 +580,16 @@ bool tc_supported(const TcLaunch& L) {
 }
 
 cudaError_t launch_tc_single_item(int B, int* n_uniq, int* uniq_e, int* uniq_off, int* ent, cudaStream_t s) {
-  tc_single_item_kernel<<<1, 256, 0, s>>>(B, n_uniq, uniq_e, uniq_off, ent);
-  return cudaGetLastError();
+  return launch_kernel(tc_single_item_kernel, dim3(1), dim3(256), 0, s, B, n_uniq, uniq_e, uniq_off, ent);
 }
 
 cudaError_t launch_tc_plan(const TcPlanArgs& a, cudaStream_t s) {
-  tc_plan_kernel<<<1, 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(tc_plan_kernel, dim3(1), dim3(32), 0, s, a);
 }
 
 cudaError_t launch_tc_pack(const TcPackArgs& a, int max_entries, cudaStream_t s) {
   if (max_entries <= 0) return cudaSuccess;
-  tc_pack_kernel<<<max_entries, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(tc_pack_kernel, dim3(max_entries), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_tc_contract(const TcLaunch& L, int mode, cudaStream_t s) {
@@ -624,8 +631,7 @@ cudaError_t launch_tc_contract(const TcLaunch& L, int mode, cudaStream_t s) {
   const long long max_units = (long long)L.max_chunks * a.tiles;
   const int grid = (int)(max_units < sms ? max_units : sms);
   if (grid <= 0) return cudaSuccess;
-  tc_contract_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(mc, ms, mcs, mss, mb, a);
-  return cudaGetLastError();
+  return launch_kernel(tc_contract_kernel, dim3(grid), dim3(kTcThreads), kSmemBytes, s, mc, ms, mcs, mss, mb, a);
 }
 
 }  // namespace tc
