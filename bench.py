@@ -135,9 +135,9 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
-def kernel_source_sha():
+def kernel_source_sha(files=("moe_decode_b1.cu", "moe_device.cuh", "moe_kernels.cu")):
     h = hashlib.sha256()
-    for f in ("moe_decode_b1.cu", "moe_device.cuh", "moe_kernels.cu"):
+    for f in files:
         with open(os.path.join(ROOT, "bit_expert_matvec_moe_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -152,6 +152,24 @@ def profiled_traffic(name):
             p = json.load(f)
         if p.get("source_sha") == kernel_source_sha():
             return p.get("dram_bytes_per_launch")
+    except Exception:  # noqa: BLE001
+        pass
+    return None
+
+
+TC_SOURCES = ("moe_tc.cu", "moe_tc.cuh", "moe_device.cuh")
+
+
+def profiled_tc_traffic(experts_per_call):
+    """dram bytes of one call's two contraction launches (gate/up + down), from
+    the committed small-pool capture scaled by the experts the call streams
+    (each expert's tiles are read once per call), if it was taken on the
+    current sources; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "tc_contract_b128.json")) as f:
+            p = json.load(f)
+        if p.get("source_sha") == kernel_source_sha(TC_SOURCES):
+            return int(round(p["dram_bytes_per_expert_per_call"] * experts_per_call))
     except Exception:  # noqa: BLE001
         pass
     return None
@@ -344,7 +362,8 @@ def run_ours(args, rank, world, local):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4) if achieved else None,
             "algorithmic_bytes_per_launch": alg,
-            "traffic": profiled_traffic("decode_b1_full_b1") if (B == 1 and bits == 4) else None,
+            "traffic": (profiled_traffic("decode_b1_full_b1") if (B == 1 and bits == 4) else
+                        profiled_tc_traffic(uniq + 1) if (tc and bits == 4) else None),
         },
         "e2e": {"value": round(job_throughput(T, world, e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_pin.numel() * 4), "d2h_bytes_per_step": int(y_pin.numel() * 4 + idx_pin.numel() * 4)},

@@ -41,6 +41,8 @@
 // copied before griddepcontrol.wait, i.e. while the previous kernel on the
 // stream may still run; nothing the caller writes (h, offsets, workspace) is
 // read before that wait.
+#include <type_traits>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -165,7 +167,7 @@ __device__ __forceinline__ void slice_rows2(const uint8_t* base, int stride, int
 
 }  // namespace
 
-template <bool kPDL>
+template <bool kPDL, int kRB, int kSB>
 __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a) {
   // every piece of block scratch lives in the planned dynamic region, whose
   // base is rounded up here to 128 bytes (the plan reserves the slack)
@@ -184,12 +186,15 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
 
   // formats by value (4-bit and 2-bit), so that no per-expert choice needs memory
   const Fmt f4 = make_fmt(4, H, I), f2 = make_fmt(2, H, I);
-  const int s_gu_pair = a.shared_bits == 4 ? f4.gu_pair : f2.gu_pair;
-  const int s_d_row = a.shared_bits == 4 ? f4.d_row : f2.d_row;
-  const size_t s_d_off = a.shared_bits == 4 ? f4.d_off : f2.d_off;
-  const int r_gu_pair = a.bits == 4 ? f4.gu_pair : f2.gu_pair;
-  const int r_d_row = a.bits == 4 ? f4.d_row : f2.d_row;
-  const size_t r_d_off = a.bits == 4 ? f4.d_off : f2.d_off;
+  // code widths are template arguments (routed kRB, shared kSB): each
+  // instantiation holds only the unpacking code it runs, which keeps the
+  // kernel's instruction footprint down
+  const int s_gu_pair = kSB == 4 ? f4.gu_pair : f2.gu_pair;
+  const int s_d_row = kSB == 4 ? f4.d_row : f2.d_row;
+  const size_t s_d_off = kSB == 4 ? f4.d_off : f2.d_off;
+  const int r_gu_pair = kRB == 4 ? f4.gu_pair : f2.gu_pair;
+  const int r_d_row = kRB == 4 ? f4.d_row : f2.d_row;
+  const size_t r_d_off = kRB == 4 ? f4.d_off : f2.d_off;
 
   uint8_t* const G = sm + a.plan.off_g;
   uint8_t* const D = sm + a.plan.off_dn;
@@ -355,11 +360,12 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     // part[p][r * chunks + chunk]; the warp waits for the slice itself.  The
     // skip test is warp-uniform: the wait and the row reductions are warp
     // collectives, so a warp takes part with all of its lanes or not at all.
-    auto gate_up = [&](int p, const uint8_t* slot, int bits, const Limbs& xl, float2 xe) {
+    auto gate_up = [&](int p, const uint8_t* slot, auto bits_c, const Limbs& xl, float2 xe) {
+      constexpr int kBits = decltype(bits_c)::value;
       if (nr == 0 || gr_warp >= 2 * nr) return;  // no rows for this warp: nothing to wait for
       if (!warp_wait(1 + p)) return;
       float o0, o1;
-      if (bits == 4)
+      if constexpr (kBits == 4)
         slice_rows2<4, true>(slot, f4.gu_row, f4.gu_codes, ngh, gg, ggact, xl, xe, gr_first, gr_step, 2 * nr,
                              mh.lpr, o0, o1);
       else
@@ -421,7 +427,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       Limbs xl;
       float2 xe;
       load_x(xl, xe);
-      gate_up(0, G + a.plan.off_sgu, a.shared_bits, xl, xe);
+      gate_up(0, G + a.plan.off_sgu, std::integral_constant<int, kSB>{}, xl, xe);
     }
     {
       // ---- routing, by warp 0 of every block (same logits, same result); the
@@ -514,7 +520,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       float2 xe;
       load_x(xl, xe);
       for (int k = 0; k < K; ++k) {
-        gate_up(hs + k, G + (size_t)k * gu_slot, a.bits, xl, xe);
+        gate_up(hs + k, G + (size_t)k * gu_slot, std::integral_constant<int, kRB>{}, xl, xe);
         if (tid == 0) STAMP(8 + k);
         // routed down rows are needed last: warp 0 issues expert k's copy once
         // its gate/up rows have landed (warp 0 has gate/up rows whenever the
@@ -652,21 +658,22 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         load_limbs(AL + (size_t)p * ngi * kLimbBytes, ngi, g, L);
         const float2 es = AE[(size_t)p * ngi + g];
         const uint8_t* base = D + (size_t)p * dn_slot;
-        const bool b4 = (p < hs ? a.shared_bits : a.bits) == 4;
         // up to kDnRows independent rows per thread, interleaved for ILP
-        if (b4) {
+        auto rows = [&](auto bits_c) {
+          constexpr int kBits = decltype(bits_c)::value;
+          const Fmt& f = kBits == 4 ? f4 : f2;
 #pragma unroll
           for (int k = 0; k < kDnRows; ++k) {
             const int r = set + k * S;
-            if (r < nj) pdn[r * Q + q] = row_group<4>(base + (size_t)r * f4.d_row, ngi, f4.d_codes, g, L, es);
+            if (r < nj) pdn[r * Q + q] = row_group<kBits>(base + (size_t)r * f.d_row, ngi, f.d_codes, g, L, es);
           }
-        } else {
-#pragma unroll
-          for (int k = 0; k < kDnRows; ++k) {
-            const int r = set + k * S;
-            if (r < nj) pdn[r * Q + q] = row_group<2>(base + (size_t)r * f2.d_row, ngi, f2.d_codes, g, L, es);
-          }
-        }
+        };
+        if constexpr (kSB == kRB)
+          rows(std::integral_constant<int, kRB>{});
+        else if (p < hs)
+          rows(std::integral_constant<int, kSB>{});
+        else
+          rows(std::integral_constant<int, kRB>{});
       }
       if (failed()) goto cleanup;
       if (tid == 0) STAMP(21);
@@ -777,11 +784,27 @@ bool decode_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_
   return decode_plan_for(nsm, optin, H, I, E, K, bits, shared_bits, has_shared, has_gate, out);
 }
 
+namespace {
+template <bool kPDL>
+using DecodeKernel = void (*)(DecodeArgs);
+// the instantiation for (PDL, routed bits, shared bits); without a shared
+// expert the shared width is the routed one
+template <bool kPDL>
+DecodeKernel<kPDL> decode_kernel_for(int bits, int shared_bits) {
+  if (bits == 4) return shared_bits == 4 ? decode_b1_kernel<kPDL, 4, 4> : decode_b1_kernel<kPDL, 4, 2>;
+  return shared_bits == 4 ? decode_b1_kernel<kPDL, 2, 4> : decode_b1_kernel<kPDL, 2, 2>;
+}
+}  // namespace
+
 cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s) {
-  static std::atomic<int> configured[2][kMaxDevices];  // per PDL variant and device
+  static std::atomic<int> configured[2][4][kMaxDevices];  // per PDL variant, code widths and device
   const int bytes = (int)a.plan.total;
-  const cudaError_t e = pdl ? ensure_dynamic_smem(decode_b1_kernel<true>, bytes, configured[1])
-                            : ensure_dynamic_smem(decode_b1_kernel<false>, bytes, configured[0]);
+  const int sb = a.has_shared ? a.shared_bits : a.bits;
+  const int v = (a.bits == 4 ? 0 : 2) + (sb == 4 ? 0 : 1);
+  const DecodeKernel<true> kp = decode_kernel_for<true>(a.bits, sb);
+  const DecodeKernel<false> kn = decode_kernel_for<false>(a.bits, sb);
+  const cudaError_t e = pdl ? ensure_dynamic_smem(kp, bytes, configured[1][v])
+                            : ensure_dynamic_smem(kn, bytes, configured[0][v]);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.plan.P);
@@ -800,7 +823,7 @@ cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return pdl ? cudaLaunchKernelEx(&cfg, decode_b1_kernel<true>, a) : cudaLaunchKernelEx(&cfg, decode_b1_kernel<false>, a);
+  return pdl ? cudaLaunchKernelEx(&cfg, kp, a) : cudaLaunchKernelEx(&cfg, kn, a);
 }
 
 }  // namespace moe
