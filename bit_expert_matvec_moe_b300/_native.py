@@ -30,6 +30,7 @@ EXPORTS = (
     "moe_expert_forward",
     "moe_layer_decode",
     "moe_layer_decode_noalloc",
+    "moe_noalloc_test_timeout_next",
     "moe_get_device_status",
     "moe_status_string",
     "moe_last_error_message",
@@ -90,6 +91,8 @@ def load() -> ctypes.CDLL:
     lib.moe_layer_decode.argtypes = [P(moe_layer), VP, I32, VP, VP, VP, VP, SZ, VP]
     lib.moe_layer_decode_noalloc.restype = ctypes.c_int
     lib.moe_layer_decode_noalloc.argtypes = [P(moe_layer), VP, VP, VP, VP, VP, VP]
+    lib.moe_noalloc_test_timeout_next.restype = ctypes.c_int
+    lib.moe_noalloc_test_timeout_next.argtypes = []
     lib.moe_get_device_status.restype = ctypes.c_int
     lib.moe_get_device_status.argtypes = [VP, VP]
     lib.moe_status_string.restype = ctypes.c_char_p

@@ -14,6 +14,8 @@
 #include <string>
 
 #include "../../include/moe.h"
+#include <cstddef>
+
 #include "moe_internal.h"
 
 using namespace moe;
@@ -28,6 +30,7 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+thread_local bool t_test_timeout_next = false;  // moe_noalloc_test_timeout_next
 
 moe_status fail(cudaError_t e, const char* what) {
   set_last_error(std::string(what) + ": " + cudaGetErrorString(e));
@@ -114,6 +117,14 @@ moe_status moe_layer_decode_noalloc(const moe_layer* layer, float* h, const floa
   // each call starts with a clear error state (the launch counters live on)
   e = cudaMemsetAsync(base, 0, kHeaderErrorBytes, s);
   if (e != cudaSuccess) return fail(e, "cudaMemsetAsync");
+  if (t_test_timeout_next) {
+    // test hook, one call: every cross-block wait of this launch expects a
+    // later epoch (header bar_extra = 1), so each block gives up after its
+    // bounded wait and the call reports a timeout
+    t_test_timeout_next = false;
+    e = cudaMemsetAsync(base + offsetof(WsHeader, bar_extra), 1, 1, s);
+    if (e != cudaSuccess) return fail(e, "cudaMemsetAsync");
+  }
 
   DecodeArgs f{};
   f.H = d.hidden;
@@ -145,6 +156,11 @@ moe_status moe_layer_decode_noalloc(const moe_layer* layer, float* h, const floa
   // caller cannot reach the array, and the next call clears it
   e = cudaMemcpyAsync(status_out, base, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return fail(e, "cudaMemcpyAsync");
+  return MOE_OK;
+}
+
+moe_status moe_noalloc_test_timeout_next(void) {
+  t_test_timeout_next = true;
   return MOE_OK;
 }
 

@@ -249,6 +249,14 @@ moe_status moe_layer_decode_noalloc(const moe_layer* layer, float* h, const floa
                                     int32_t* idx_out, float* w_out, int32_t* status_out,
                                     moe_stream_t stream);
 
+/* Test hook (no counterpart on the pages): the next moe_layer_decode_noalloc
+ * call made by this thread sets its array's test word so that every
+ * cross-block wait of that launch expects a later launch's data; each block
+ * then gives up after its bounded wait (1 s) and the call's status_out
+ * receives the timeout bit.  No GPU fault, trap or endless wait is involved.
+ * The call after that runs normally.  Returns MOE_OK. */
+moe_status moe_noalloc_test_timeout_next(void);
+
 /* Static text of a status code. */
 const char* moe_status_string(moe_status s);
 

@@ -104,3 +104,33 @@ def test_noalloc_requires_a_status_word():
     st = lib.moe_layer_decode_noalloc(ctypes.byref(layer), h.data_ptr(), None, None, None, None,
                                       torch.cuda.current_stream().cuda_stream)
     assert st == N.MOE_ERR_INVALID_ARG
+
+
+def test_noalloc_timeout_is_reported_then_the_next_call_recovers():
+    """The path unique to this entry point: a bounded cross-block wait runs out
+    (the library's one-shot test hook makes every wait of the launch expect a
+    later launch's data; each block gives up after 1 s, no fault), status_out
+    carries the timeout bit, and the next call - which clears the error state
+    of the array itself - matches moe_layer_decode and the oracle."""
+    from bit_expert_matvec_moe_b300 import _native as N
+
+    L = build_layer(M.Dims(flags=M.MOE_HAS_SHARED, hidden=256, inter=128, n_experts=16, top_k=4))
+    hs = G.hidden_states(G.SEED, 43, 2, 256)
+    assert N.load().moe_noalloc_test_timeout_next() == 0
+    h = torch.from_numpy(hs[0:1].copy()).cuda()
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    M.moe_layer_decode_noalloc(L.c_layer(), h, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1  # ST_TIMEOUT
+    # the following call runs normally on the same array
+    y_ref, idx_ref, w_ref = _decode_with_workspace(L, hs[1:2])
+    y, idx, w = _decode_noalloc(L, hs[1:2])
+    assert np.array_equal(idx, idx_ref)
+    assert rel_err(w, w_ref) <= REL_TOL
+    assert rel_err(y[0], y_ref[0]) <= REL_TOL
+    ref = L.oracle(hs[1])
+    ok, tie = routing_ok(idx[0], ref["logits"], L.dims.top_k)
+    assert ok
+    if tie:
+        ref = L.oracle(hs[1], force_chosen=idx[0])
+    assert rel_err(y[0], ref["y"]) <= REL_TOL
