@@ -269,6 +269,39 @@ def test_pdl_back_to_back_calls_match_oracle(full4):
     assert rel_err(h.cpu().numpy()[0], ref) <= REL_TOL
 
 
+@pytest.mark.parametrize("tc", [False, True])
+def test_pdl_batched_chain_matches_plain_launches(full4, tc):
+    """Batched calls (B = 8) queued back to back with every kernel of the
+    multi-kernel path chained by programmatic dependent launch, each call
+    reading the h the previous call wrote: the results equal those of plain
+    launches bit for bit (same kernels, same order of arithmetic), and the
+    first call matches the oracle at every token."""
+    B, n = 8, 3
+    h0 = G.hidden_states(G.SEED, 22, B, 4096)
+    off = np.tile(G.popularity_offsets(G.SEED, 0, 512), (B, 1))
+    extra = M.MOE_TENSOR_CORES if tc else 0
+    outs = {}
+    for pdl in (False, True):
+        d = M.Dims(**{**full4.dims.__dict__, "flags": full4.dims.flags | extra | (M.MOE_PDL if pdl else 0)})
+        layer = M.make_layer(d, full4.experts, full4.stride, full4.router, shared=full4.shared, shared_bits=4)
+        h = torch.from_numpy(h0.copy()).cuda()
+        o = torch.from_numpy(off).cuda()
+        ws = workspace(d, B)
+        idx = torch.empty((B, 4), dtype=torch.int32, device="cuda")
+        w = torch.empty((B, 4), dtype=torch.float32, device="cuda")
+        ys = []
+        for c in range(n):
+            M.moe_layer_decode(layer, h, ws, logit_offset=o, idx_out=idx if c == 0 else None,
+                               w_out=w if c == 0 else None)
+            ys.append(h.clone())
+        assert M.moe_get_device_status(ws) == 0
+        outs[pdl] = ([y.cpu().numpy() for y in ys], idx.cpu().numpy(), w.cpu().numpy())
+    for a, b in zip(outs[False][0], outs[True][0]):
+        assert np.array_equal(a, b)
+    assert np.array_equal(outs[False][1], outs[True][1])
+    check_batch(full4, h0, outs[True][0][0], outs[True][1], outs[True][2], offset=off)
+
+
 def test_fused_is_deterministic(full4):
     h = G.hidden_states(G.SEED, 5, 1, 4096)
     y1, i1, w1 = decode(full4, h)
