@@ -17,10 +17,12 @@
 //   h -> limbs of h*gamma (the RMS factor r multiplies each gate/up dot
 //        product, so quantisation does not wait for the norm); r from a block sum
 //   router rows -> published logits
-//   shared expert gate/up (all warps)
-//   warp 0: poll every block's logits (16 words per lane in flight); top-K
-//           (every block, same result);
-//           issue the routed gate/up copies; softmax over the chosen
+//   warps 1..: shared expert gate/up.  Meanwhile warp 0: poll every block's
+//           logits (16 words per lane in flight); top-K (every block, same
+//           result); issue the routed gate/up copies whose slots do not
+//           overlap the shared slice; softmax over the chosen; then its own
+//           shared rows and, once every warp is done with the shared slice,
+//           the remaining copies
 //   routed gate/up rows expert by expert as their copies land
 //   SwiGLU of every expert's rows, times its routing weight -> published
 //   wait for the activation counter; every thread loads its 12 words straight
@@ -422,22 +424,45 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       }
     }
 
-    // ---- shared expert gate/up (its rows were staged first)
-    if (hs) {
-      Limbs xl;
-      float2 xe;
-      load_x(xl, xe);
-      gate_up(0, G + a.plan.off_sgu, std::integral_constant<int, kSB>{}, xl, xe);
-    }
+    // routed gate/up copies of experts k0 .. k1 - 1 (lane 0 of warp 0)
+    auto issue_routed = [&](int k0, int k1) {
+      uint32_t issued = s_mask[0];
+      for (int k = k0; k < k1; ++k) {
+        const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
+        if (nr > 0) {
+          const uint32_t bytes = (uint32_t)nr * r_gu_pair;
+          mbar_expect_tx(&bar[1 + hs + k], bytes);
+          bulk_g2s(G + (size_t)k * gu_slot, blob + (size_t)r0 * r_gu_pair, bytes, &bar[1 + hs + k]);
+          issued |= 2u << (hs + k);
+        }
+      }
+      s_mask[0] = issued;
+    };
+    // ---- shared expert gate/up (its rows were staged first): warps 1.. now,
+    // warp 0 once it has routed the token (below)
+    auto shared_gate_up = [&]() {
+      if (hs) {
+        Limbs xl;
+        float2 xe;
+        load_x(xl, xe);
+        gate_up(0, G + a.plan.off_sgu, std::integral_constant<int, kSB>{}, xl, xe);
+      }
+    };
+    // Routed gate/up slice k goes to slot k of the gate/up area.  Slots that do
+    // not overlap the shared slice (the router rows and h there are dead once
+    // the logits are out) are copied right after top-K; slots 0 .. k_late - 1,
+    // which the shared slice covers, once every warp is done with it.
+    const size_t shared_end = hs ? a.plan.off_sgu + (size_t)nr * s_gu_pair : 0;
+    const int k_late = min(K, (int)((shared_end + gu_slot - 1) / gu_slot));
     {
-      // ---- routing, by warp 0 of every block (same logits, same result); the
-      // other warps go on to wait for the routed rows.  The routed copies
-      // overwrite the gate/up area, so warp 0 issues them only after every
-      // warp has finished with the shared rows (named barrier 1: the other
-      // warps arrive without waiting).
-      if (wid != 0) named_arrive(1, kBlock);
+      // ---- routing, by warp 0 of every block (same logits, same result),
+      // while the other warps compute the shared rows; they then arrive on
+      // named barrier 1 without waiting and go on to the routed rows.
+      if (wid != 0) {
+        shared_gate_up();
+        named_arrive(1, kBlock);
+      }
       if (wid == 0) {
-        named_sync(1, kBlock);
         if (lane == 0) STAMP(5);
         bool ok = true;
         bool ready = true;  // the words carry their epoch: polled directly
@@ -483,20 +508,10 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
           }
           ok = __all_sync(0xffffffffu, ok);
           if (lane == 0) {
-            // the generic-proxy reads of the gate/up area are complete (block
-            // barrier after the router rows, named barrier after the shared rows)
+            // the generic-proxy reads of the router rows and h are complete
+            // (block barrier after the router rows)
             fence_proxy_async();
-            uint32_t issued = s_mask[0];
-            for (int k = 0; k < K; ++k) {
-              const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
-              if (nr > 0) {
-                const uint32_t bytes = (uint32_t)nr * r_gu_pair;
-                mbar_expect_tx(&bar[1 + hs + k], bytes);
-                bulk_g2s(G + (size_t)k * gu_slot, blob + (size_t)r0 * r_gu_pair, bytes, &bar[1 + hs + k]);
-                issued |= 2u << (hs + k);
-              }
-            }
-            s_mask[0] = issued;
+            issue_routed(k_late, K);
             STAMP(7);
             chosen_softmax(s_val, K, s_coef + hs);
             if (hs) s_coef[0] = a.has_gate ? 1.0f / (1.0f + expf(-gate_logit)) : 1.0f;
@@ -512,6 +527,16 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
           atomicOr(&s_mask[1], 1u);
         }
         __syncwarp();
+        // this warp's shared rows, then the copies over the shared slice once
+        // every warp is done with it (only if routing succeeded: s_idx is
+        // written by top-K)
+        shared_gate_up();
+        named_sync(1, kBlock);
+        if (lane == 0 && k_late > 0 && *(volatile uint32_t*)&s_mask[1] == 0u) {
+          fence_proxy_async();  // the generic-proxy reads of the shared rows are complete
+          issue_routed(0, k_late);
+        }
+        __syncwarp();
       }
     }
     {
@@ -519,9 +544,10 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       Limbs xl;
       float2 xe;
       load_x(xl, xe);
-      for (int k = 0; k < K; ++k) {
+      for (int i = 0; i < K; ++i) {
+        const int k = (i + k_late) % K;  // early slots first, as their copies went out
         gate_up(hs + k, G + (size_t)k * gu_slot, std::integral_constant<int, kRB>{}, xl, xe);
-        if (tid == 0) STAMP(8 + k);
+        if (tid == 0) STAMP(8 + i);
         // routed down rows are needed last: warp 0 issues expert k's copy once
         // its gate/up rows have landed (warp 0 has gate/up rows whenever the
         // block has any, and gate_up waited for them), which keeps the copies
