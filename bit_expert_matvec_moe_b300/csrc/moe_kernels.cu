@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kRtThreads) router_kernel(RouterArgs a) {
 // softmax / top-K / renormalise per token: one warp per token
 // ---------------------------------------------------------------------------
 constexpr int kTopkPer = 32;  // experts per lane: up to 1024 experts
-constexpr int kTopkThreads = 256;
+constexpr int kTopkThreads = 512;  // one logit per thread up to 512 experts
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   pdl_wait_prior();  // no-op unless launched with programmatic serialisation
   pdl_launch_dependents();
@@ -275,12 +275,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   for (int e = tid; e < nrows; e += blockDim.x) {
     float v = part[e];
     int sp = 1;
-    for (; sp + 8 <= a.splits; sp += 8) {  // eight loads in flight, added in split order
-      float p[8];
+    for (; sp + 16 <= a.splits; sp += 16) {  // sixteen loads in flight, added in split order
+      float p[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) p[i] = part[(size_t)(sp + i) * pstride + e];
+      for (int i = 0; i < 16; ++i) p[i] = part[(size_t)(sp + i) * pstride + e];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v += p[i];
+      for (int i = 0; i < 16; ++i) v += p[i];
     }
     for (; sp < a.splits; ++sp) v += part[(size_t)sp * pstride + e];
     if (e < a.E && a.offset) v += a.offset[(size_t)b * a.E + e];
