@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--experts", type=int, default=512, help="routed experts (smaller pools for profiling runs)")
     p.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch between decode calls")
+    p.add_argument("--per-layer", action="store_true",
+                   help="40-layer stack: one moe_layer_decode call per layer instead of one moe_stack_decode per token")
     p.add_argument("--tensor-cores", action="store_true",
                    help="B > 1: expert contractions on the tensor cores (MOE_TENSOR_CORES)")
     return p.parse_args()
@@ -387,7 +389,9 @@ def run_ours(args, rank, world, local):
 # ----------------------------------------------------------------------------- 40-layer stack
 def run_stack(args, rank, world, local):
     """40 full-width 4-bit layers resident in HBM; each token passes all of them
-    (RMSNorm before, residual after each, inside every layer call).  Every layer
+    (RMSNorm before, residual after each), one moe_stack_decode call per token
+    (every layer in one launch), or with --per-layer one moe_layer_decode call
+    per layer.  Every layer
     has its own copy of the 512-expert pool, shared expert and router (identical
     bytes, distinct addresses: 145 GB of experts), so nothing a token reads is
     left in L2 by the previous token.  Routing follows a reuse trace (token t's
@@ -415,31 +419,34 @@ def run_stack(args, rank, world, local):
     routers = [router0[0]] + [router0[0].clone() for _ in range(Lyr - 1)]
     layers = [M.make_layer(d, pools[l], stride, routers[l], shared=shared[l], shared_bits=4) for l in range(Lyr)]
     trace = np.stack([G.reuse_trace(G.SEED, l, T, E, K) for l in range(Lyr)])  # [L, T, K]
-    offs_h = np.zeros((Lyr, T, E), dtype=np.float32)
+    offs_h = np.zeros((T, Lyr, E), dtype=np.float32)  # token t's rows: one per layer
     for l in range(Lyr):
         for t in range(T):
-            offs_h[l, t] = G.trace_offsets(trace[l, t], E)
+            offs_h[t, l] = G.trace_offsets(trace[l, t], E)
     offs = torch.from_numpy(offs_h).cuda()
     h_host = G.hidden_states(G.SEED, 100 + rank, T, d.hidden)
     h0 = torch.from_numpy(h_host).cuda()
     h = h0.clone()
     ws = torch.empty(M.moe_workspace_bytes(d, 1), dtype=torch.uint8, device="cuda")
     M.moe_workspace_init(ws)
-    idx = torch.empty((Lyr, T, K), dtype=torch.int32, device="cuda")
+    idx = torch.empty((T, Lyr, K), dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
     def one_step():
         for t in range(T):
-            for l in range(Lyr):
-                M.moe_layer_decode(layers[l], h[t:t + 1], ws, logit_offset=offs[l, t:t + 1], idx_out=idx[l, t:t + 1],
-                                   stream=stream)
+            if args.per_layer:
+                for l in range(Lyr):
+                    M.moe_layer_decode(layers[l], h[t:t + 1], ws, logit_offset=offs[t, l:l + 1],
+                                       idx_out=idx[t, l:l + 1], stream=stream)
+            else:
+                M.moe_stack_decode(layers, h[t:t + 1], ws, logit_offset=offs[t], idx_out=idx[t], stream=stream)
 
     with torch.cuda.stream(stream):
         one_step()
     assert M.moe_get_device_status(ws, stream) == 0
     got = np.sort(idx.cpu().numpy(), axis=-1)
-    assert np.array_equal(got, np.sort(trace, axis=-1)), "routing does not follow the imposed trace"
+    assert np.array_equal(got, np.sort(trace.transpose(1, 0, 2), axis=-1)), "routing does not follow the imposed trace"
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         one_step()
@@ -484,6 +491,7 @@ def run_stack(args, rank, world, local):
                 e2e_ms.append(e0.elapsed_time(e1))
     e2e = max_over_ranks(float(np.mean(e2e_ms)), world, "cuda")
     layer_bytes = (K + 1) * M.moe_packed_expert_bytes(d, 4) + E * d.hidden * 2
+    launches = T * Lyr if args.per_layer else T * -(-Lyr // 64)
     tok_s = job_throughput(T, world, ms)
     per_launch_s = ms / 1e3 / (T * Lyr)
     peak, peak_kind = measured_hbm_peak()
@@ -505,7 +513,8 @@ def run_stack(args, rank, world, local):
         "config": {
             "workload": (f"{Lyr}-layer MoE decode stack resident in HBM: full-width 4-bit layers (hidden 4096, {E} experts, "
                          f"top-4 + 1 shared, inter 1024), {T} tokens, top-4 reuse trace p=0.27"),
-            "batch": 1, "tokens_per_step": T, "layers": Lyr, "launches_per_step": T * Lyr,
+            "batch": 1, "tokens_per_step": T, "layers": Lyr, "launches_per_step": launches,
+            "entry": "moe_layer_decode per layer" if args.per_layer else "moe_stack_decode per token",
             "l2": "no reuse: every layer has its own expert pool, shared expert and router (145 GB of experts)",
             "graph": True, "parallelism": f"replicas x{world}",
         },
@@ -513,13 +522,14 @@ def run_stack(args, rank, world, local):
         "us_per_layer": round(per_launch_s * 1e6, 3),
         "bytes_per_token": int(layer_bytes * Lyr),
         "roofline": {
-            "bound": "hbm", "kernel": "decode_b1_kernel", "achieved": round(achieved, 1), "peak": peak,
+            "bound": "hbm", "kernel": "decode_b1_kernel" if args.per_layer else "decode_stack_kernel",
+            "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "algorithmic_bytes_per_launch": int(layer_bytes), "traffic": None,
+            "algorithmic_bytes_per_launch": int(layer_bytes * (T * Lyr // launches)), "traffic": None,
         },
         "e2e": {"value": round(job_throughput(T, world, e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_pin.numel() * 4), "d2h_bytes_per_step": int(y_pin.numel() * 4)},
-        "gpu_launches": T * Lyr * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": ck,
     }
     print(f"# {tok_s:.1f} tokens/s through {Lyr} layers, {per_launch_s * 1e6:.3f} us/layer", file=sys.stderr, flush=True)

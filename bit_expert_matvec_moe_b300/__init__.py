@@ -16,7 +16,8 @@ from ._native import MOE_HAS_SHARED, MOE_HAS_SHARED_GATE, MOE_NO_FUSED, MOE_PDL,
 
 __all__ = [
     "Dims", "MoeError", "moe_packed_expert_bytes", "moe_workspace_bytes", "moe_workspace_init",
-    "moe_pack_weights", "moe_route", "moe_expert_forward", "moe_layer_decode", "moe_layer_decode_noalloc",
+    "moe_pack_weights", "moe_route", "moe_expert_forward", "moe_layer_decode", "moe_stack_decode",
+    "moe_layer_decode_noalloc",
     "moe_get_device_status",
     "make_layer",
 ]
@@ -175,6 +176,24 @@ def moe_layer_decode(layer: N.moe_layer, h, ws, logit_offset=None, idx_out=None,
     _check(N.load().moe_layer_decode(ctypes.byref(layer), ph, B, po, pi, pw, _ptr(ws), ws.numel() * ws.element_size(),
                                      _stream(stream)),
            "moe_layer_decode")
+
+
+def moe_stack_decode(layers, h, ws, logit_offset=None, idx_out=None, w_out=None, stream=None) -> None:
+    """One token through the layers in order, in place on h ([1, hidden] or
+    [hidden]).  layers: a sequence of moe_layer of equal dims; logit_offset
+    [n_layers, n_experts], idx_out / w_out [n_layers, top_k] (or None)."""
+    layers = list(layers)
+    if not layers:
+        raise ValueError("moe_stack_decode: no layers")
+    d = layers[0].d
+    n = len(layers)
+    if h.numel() != d.hidden:
+        raise ValueError(f"moe_stack_decode: h must hold one token ({d.hidden} values)")
+    arr = (N.moe_layer * n)(*layers)
+    ph, po, pi, pw = _ptrs((h, "h", "f32", d.hidden), (logit_offset, "logit_offset", "f32", n * d.n_experts),
+                           (idx_out, "idx_out", "i32", n * d.top_k), (w_out, "w_out", "f32", n * d.top_k))
+    _check(N.load().moe_stack_decode(arr, n, ph, po, pi, pw, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_stack_decode")
 
 
 def moe_layer_decode_noalloc(layer: N.moe_layer, h, status_out, logit_offset=None, idx_out=None, w_out=None,

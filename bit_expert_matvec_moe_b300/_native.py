@@ -29,6 +29,7 @@ EXPORTS = (
     "moe_route",
     "moe_expert_forward",
     "moe_layer_decode",
+    "moe_stack_decode",
     "moe_layer_decode_noalloc",
     "moe_noalloc_test_timeout_next",
     "moe_get_device_status",
@@ -89,6 +90,8 @@ def load() -> ctypes.CDLL:
     lib.moe_expert_forward.argtypes = [P(moe_dims), I32, VP, VP, I32, VP, VP, I32, VP, SZ, VP]
     lib.moe_layer_decode.restype = ctypes.c_int
     lib.moe_layer_decode.argtypes = [P(moe_layer), VP, I32, VP, VP, VP, VP, SZ, VP]
+    lib.moe_stack_decode.restype = ctypes.c_int
+    lib.moe_stack_decode.argtypes = [P(moe_layer), I32, VP, VP, VP, VP, VP, SZ, VP]
     lib.moe_layer_decode_noalloc.restype = ctypes.c_int
     lib.moe_layer_decode_noalloc.argtypes = [P(moe_layer), VP, VP, VP, VP, VP, VP]
     lib.moe_noalloc_test_timeout_next.restype = ctypes.c_int

@@ -50,7 +50,7 @@ bool dims_ok(const moe_dims* d) {
 }
 
 struct WsLayout {
-  size_t logits, idx, w, gs, xn, xq, xe, a, aq, ae, d, nuniq, uniq_e, uniq_off, ent, pub_logits, pub_act;
+  size_t logits, idx, w, gs, xn, xq, xe, a, aq, ae, d, nuniq, uniq_e, uniq_off, ent, pub_logits, pub_act, pub_h;
   // tensor-core contraction (MOE_TENSOR_CORES only): B operand rows and scales, work list
   size_t xops, aops, xscale, ascale, chunks, nchunks;
   int max_chunks;
@@ -75,6 +75,7 @@ WsLayout ws_layout(const moe_dims& d, int B) {
   // depend on the batch (epoch << 32 | value)
   L.pub_logits = take((size_t)(MOE_MAX_EXPERTS + 1) * 8);
   L.pub_act = take(ns * I * 8);
+  L.pub_h = take((H + 127) / 128 * 128 * 8);  // a stack launch's layer outputs (slots in chunks of 128)
   L.logits = take((size_t)router_splits(B, (int)H, (int)E) * B * (E + 1) * 4);
   L.idx = take(B * K * 4);
   L.w = take(B * K * 4);
@@ -387,24 +388,130 @@ moe_status moe_expert_forward(const moe_dims* dims, int32_t bits, const void* bl
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
-moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const float* logit_offset, int32_t* idx_out,
-                            float* w_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
-  if (!layer || !dims_ok(&layer->d) || B < 1 || B > MOE_MAX_BATCH) return MOE_ERR_INVALID_ARG;
+// A layer's own buffers and dims (the checks every layer call makes).
+static bool layer_ok(const moe_layer* layer) {
+  if (!layer || !dims_ok(&layer->d)) return false;
   const moe_dims& d = layer->d;
   const int has_shared = (d.flags & MOE_HAS_SHARED) ? 1 : 0;
   const int has_gate = (d.flags & MOE_HAS_SHARED_GATE) ? 1 : 0;
-  if (!h || !ws || !layer->experts || !layer->router) return MOE_ERR_INVALID_ARG;
-  if (has_shared && (!layer->shared || (layer->shared_bits != 4 && layer->shared_bits != 2))) return MOE_ERR_INVALID_ARG;
-  if (has_gate && !layer->shared_gate) return MOE_ERR_INVALID_ARG;
+  if (!layer->experts || !layer->router) return false;
+  if (has_shared && (!layer->shared || (layer->shared_bits != 4 && layer->shared_bits != 2))) return false;
+  if (has_gate && !layer->shared_gate) return false;
   const size_t blob = make_fmt(d.bits, d.hidden, d.inter).total;
-  if (layer->expert_stride < blob || layer->expert_stride % 16) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(h) || !aligned16(ws) || !aligned16(layer->experts) || !aligned16(layer->router) ||
-      (has_shared && !aligned16(layer->shared)) || (layer->rms_gamma && !aligned16(layer->rms_gamma)) ||
-      (has_gate && !aligned16(layer->shared_gate)) || (logit_offset && !aligned16(logit_offset)) ||
+  if (layer->expert_stride < blob || layer->expert_stride % 16) return false;
+  return aligned16(layer->experts) && aligned16(layer->router) && (!has_shared || aligned16(layer->shared)) &&
+         (!layer->rms_gamma || aligned16(layer->rms_gamma)) && (!has_gate || aligned16(layer->shared_gate));
+}
+
+// The single-token kernel's pointers of one layer.
+static DecodeLayer decode_layer_of(const moe_layer& layer, const float* logit_offset, int32_t* idx_out, float* w_out) {
+  DecodeLayer y{};
+  y.experts = static_cast<const uint8_t*>(layer.experts);
+  y.stride = layer.expert_stride;
+  y.shared = static_cast<const uint8_t*>(layer.shared);
+  y.router = layer.router;
+  y.gamma = layer.rms_gamma;
+  y.gate = layer.shared_gate;
+  y.offset = logit_offset;
+  y.idx_out = idx_out;
+  y.w_out = w_out;
+  return y;
+}
+
+// The single-token kernel's arguments (no layer) when the shape fits it.
+static bool decode_args_for(const moe_dims& d, int shared_bits, float* h, void* ws, const WsLayout& L, DecodeArgs* f) {
+  const int has_shared = (d.flags & MOE_HAS_SHARED) ? 1 : 0;
+  const int has_gate = (d.flags & MOE_HAS_SHARED_GATE) ? 1 : 0;
+  if (d.flags & MOE_NO_FUSED) return false;
+  DecodePlan plan;
+  if (!decode_plan(d.hidden, d.inter, d.n_experts, d.top_k, d.bits, shared_bits, has_shared, has_gate,
+                   current_device(), &plan))
+    return false;
+  *f = DecodeArgs{};
+  f->H = d.hidden;
+  f->I = d.inter;
+  f->E = d.n_experts;
+  f->K = d.top_k;
+  f->bits = d.bits;
+  f->shared_bits = shared_bits;
+  f->has_shared = has_shared;
+  f->has_gate = has_gate;
+  f->eps = d.rms_eps;
+  f->h = h;
+  f->hdr = at<WsHeader>(ws, 0);
+  f->pub_logits = at<unsigned long long>(ws, L.pub_logits);
+  f->pub_act = at<unsigned long long>(ws, L.pub_act);
+  f->plan = plan;
+  return true;
+}
+
+static moe_status layer_decode_checked(const moe_layer* layer, float* h, int32_t B, const float* logit_offset,
+                                       int32_t* idx_out, float* w_out, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream);
+
+moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const float* logit_offset, int32_t* idx_out,
+                            float* w_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!layer_ok(layer) || B < 1 || B > MOE_MAX_BATCH) return MOE_ERR_INVALID_ARG;
+  if (!h || !ws || !aligned16(h) || !aligned16(ws) || (logit_offset && !aligned16(logit_offset)) ||
       (idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out)))
     return MOE_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(d, B);
+  if (ws_bytes < ws_layout(layer->d, B).total) return MOE_ERR_INVALID_ARG;
+  return layer_decode_checked(layer, h, B, logit_offset, idx_out, w_out, ws, ws_bytes, stream);
+}
+
+moe_status moe_stack_decode(const moe_layer* layers, int32_t n_layers, float* h, const float* logit_offset,
+                            int32_t* idx_out, float* w_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!layers || n_layers < 1 || !layer_ok(&layers[0])) return MOE_ERR_INVALID_ARG;
+  const moe_dims& d = layers[0].d;
+  const int has_shared = (d.flags & MOE_HAS_SHARED) ? 1 : 0;
+  for (int l = 1; l < n_layers; ++l) {
+    const moe_dims& o = layers[l].d;
+    if (!layer_ok(&layers[l]) || o.hidden != d.hidden || o.inter != d.inter || o.n_experts != d.n_experts ||
+        o.top_k != d.top_k || o.group != d.group || o.bits != d.bits || o.rms_eps != d.rms_eps ||
+        o.flags != d.flags || (has_shared && layers[l].shared_bits != layers[0].shared_bits))
+      return MOE_ERR_INVALID_ARG;
+  }
+  // the per-layer rows of the offsets and outputs are read and written one
+  // element at a time: 4-byte alignment
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!h || !ws || !aligned16(h) || !aligned16(ws) || (logit_offset && !a4(logit_offset)) ||
+      (idx_out && !a4(idx_out)) || (w_out && !a4(w_out)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d, 1);
   if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+  const int E = d.n_experts, K = d.top_k;
+  auto row_off = [&](int l) { return logit_offset ? logit_offset + (size_t)l * E : nullptr; };
+  auto row_idx = [&](int l) { return idx_out ? idx_out + (size_t)l * K : nullptr; };
+  auto row_w = [&](int l) { return w_out ? w_out + (size_t)l * K : nullptr; };
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StackArgs sa{};
+  if (decode_args_for(d, has_shared ? layers[0].shared_bits : d.bits, h, ws, L, &sa.d)) {
+    sa.pub_h = at<unsigned long long>(ws, L.pub_h);
+    for (int l0 = 0; l0 < n_layers; l0 += kMaxStackLayers) {
+      sa.L = std::min(kMaxStackLayers, n_layers - l0);
+      for (int i = 0; i < sa.L; ++i)
+        sa.layers[i] = decode_layer_of(layers[l0 + i], row_off(l0 + i), row_idx(l0 + i), row_w(l0 + i));
+      const cudaError_t e = launch_decode_stack(sa, (d.flags & MOE_PDL) != 0, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return MOE_OK;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_status st = layer_decode_checked(&layers[l], h, 1, row_off(l), row_idx(l), row_w(l), ws, ws_bytes, stream);
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
+
+// moe_layer_decode after its argument checks.
+static moe_status layer_decode_checked(const moe_layer* layer, float* h, int32_t B, const float* logit_offset,
+                                       int32_t* idx_out, float* w_out, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream) {
+  (void)ws_bytes;
+  const moe_dims& d = layer->d;
+  const int has_shared = (d.flags & MOE_HAS_SHARED) ? 1 : 0;
+  const int has_gate = (d.flags & MOE_HAS_SHARED_GATE) ? 1 : 0;
+  const WsLayout L = ws_layout(d, B);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = at<WsHeader>(ws, 0);
   const int shared_bits = has_shared ? layer->shared_bits : d.bits;
@@ -412,37 +519,11 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B, const f
   if (tc_refused(d, B)) return MOE_ERR_UNSUPPORTED;
   const bool use_tc = B > 1 && (d.flags & MOE_TENSOR_CORES);
 
-  if (B == 1 && !(d.flags & MOE_NO_FUSED)) {
-    DecodePlan plan;
-    if (decode_plan(d.hidden, d.inter, d.n_experts, d.top_k, d.bits, shared_bits, has_shared, has_gate,
-                    current_device(), &plan)) {
-      DecodeArgs f{};
-      f.H = d.hidden;
-      f.I = d.inter;
-      f.E = d.n_experts;
-      f.K = d.top_k;
-      f.bits = d.bits;
-      f.shared_bits = shared_bits;
-      f.has_shared = has_shared;
-      f.has_gate = has_gate;
-      f.eps = d.rms_eps;
-      f.experts = static_cast<const uint8_t*>(layer->experts);
-      f.stride = layer->expert_stride;
-      f.shared = static_cast<const uint8_t*>(layer->shared);
-      f.router = layer->router;
-      f.gamma = layer->rms_gamma;
-      f.gate = layer->shared_gate;
-      f.h = h;
-      f.offset = logit_offset;
-      f.idx_out = idx_out;
-      f.w_out = w_out;
-      f.hdr = hdr;
-      f.pub_logits = at<unsigned long long>(ws, L.pub_logits);
-      f.pub_act = at<unsigned long long>(ws, L.pub_act);
-      f.plan = plan;
-      e = launch_decode(f, (d.flags & MOE_PDL) != 0, s);
-      return e == cudaSuccess ? MOE_OK : cuda_fail(e);
-    }
+  DecodeArgs f;
+  if (B == 1 && decode_args_for(d, shared_bits, h, ws, L, &f)) {
+    f.ly = decode_layer_of(*layer, logit_offset, idx_out, w_out);
+    e = launch_decode(f, (d.flags & MOE_PDL) != 0, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
   }
 
   // multi-kernel path (its kernels chained by programmatic launch with MOE_PDL)

@@ -43,6 +43,16 @@
 // copied before griddepcontrol.wait, i.e. while the previous kernel on the
 // stream may still run; nothing the caller writes (h, offsets, workspace) is
 // read before that wait.
+//
+// decode_stack_kernel runs the layers of one token in one launch, the same
+// phases once per layer.  Layer l's output rows are published like the
+// activations (epoch words, one relaxed counter) and read back by every block
+// as layer l + 1's input; each block keeps its own rows in registers for the
+// residual.  The next layer's router rows and shared gate/up rows are copied
+// as soon as the routed gate/up slices are dead (after the gate/up phase), and
+// its shared down rows once the down rows are done, so that they have landed
+// when the layer starts.  The layers' epochs are consecutive; every mbarrier
+// completes one phase per copy, its parity tracked per layer.
 #include <type_traits>
 
 #include "moe_internal.h"
@@ -67,6 +77,12 @@ __device__ unsigned long long g_timeline[1024 * kStamps];
 // reads a group (lane j takes values 4j .. 4j+3) reads 16 consecutive words per
 // load.
 __device__ __forceinline__ int act_slot(int i) { return (i & ~63) | ((i & 3) << 4) | ((i >> 2) & 15); }
+
+// Slot of output row j in a stack launch's published h: inside each chunk of
+// 128, value 4l + t goes to slot 32t + l, so that the warp that reads a chunk
+// (lane l takes values 4l .. 4l+3) reads 32 consecutive words per load.  The
+// published vector spans H rounded up to 128 words.
+__device__ __forceinline__ int h_slot(int j) { return (j & ~127) | ((j & 3) << 5) | ((j >> 2) & 31); }
 
 constexpr int kDnRows = 5;  // down rows per thread (the plan checks rows_d <= kDnRows * sets)
 
@@ -169,8 +185,17 @@ __device__ __forceinline__ void slice_rows2(const uint8_t* base, int stride, int
 
 }  // namespace
 
-template <bool kPDL, int kRB, int kSB>
-__global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a) {
+// The body of both kernels for layer l: the only layer (decode_b1_kernel), or
+// layer l of one token's layers (decode_stack_kernel, which calls it for
+// l = 0, 1, ...: layer l's output rows are published for every block and read
+// back as layer l + 1's input; the next layer's router rows and shared gate/up
+// rows are copied once the routed gate/up slices are dead, its shared down rows
+// once the down rows are done).  Every layer has its own epoch, one above the
+// previous layer's.  The launch prologue runs with layer 0.  Returns false
+// when the block gave up (the launch is then over for it).
+template <bool kPDL, int kRB, int kSB, bool kStack>
+__device__ __forceinline__ bool decode_body(const DecodeArgs& a, const DecodeLayer* layers, int nlayers,
+                                            unsigned long long* pub_h, int l) {
   // every piece of block scratch lives in the planned dynamic region, whose
   // base is rounded up here to 128 bytes (the plan reserves the slack)
   extern __shared__ uint8_t sm_raw[];
@@ -205,18 +230,55 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   float* const part = reinterpret_cast<float*>(sm + a.plan.off_part);    // [NE][part_stride]
   float* const rpart = reinterpret_cast<float*>(sm + a.plan.off_rpart);  // [rows_r][kWarps]
   float* const ysm = reinterpret_cast<float*>(sm + a.plan.off_y);        // [rows_d]
-  float* const pdn = reinterpret_cast<float*>(G);  // down partials [rows_d][NE * ngi], after the gate/up phase
+  float* const pdn = reinterpret_cast<float*>(G + a.plan.off_pdn);  // down partials [rows_d][NE * ngi]
   uint64_t* const bar = reinterpret_cast<uint64_t*>(sm + a.plan.off_bar);
   float* const s_red = reinterpret_cast<float*>(sm + a.plan.off_misc);               // [kWarps]
   int* const s_idx = reinterpret_cast<int*>(sm + a.plan.off_misc + 64);              // [kMaxTopK]
   float* const s_val = reinterpret_cast<float*>(sm + a.plan.off_misc + 96);          // [kMaxTopK]
   float* const s_coef = reinterpret_cast<float*>(sm + a.plan.off_misc + 128);        // [kMaxTopK + 1]
-  uint32_t* const s_mask = reinterpret_cast<uint32_t*>(sm + a.plan.off_misc + 168);  // issued, failed, epoch, hook, bumped, act
+  // issued, failed, epoch, hook, bumped, act wait, issued for the next layer,
+  // h wait, barrier phases (bit i: the parity of barrier i's phase in this
+  // layer; written by thread 0 at the start of a layer, always 0 for one layer)
+  uint32_t* const s_mask = reinterpret_cast<uint32_t*>(sm + a.plan.off_misc + 168);
+  // (stack) the output-row counter as this launch found it
+  unsigned long long* const s_hbase = reinterpret_cast<unsigned long long*>(sm + a.plan.off_misc + 208);
+  // the current layer's pointers: the launch argument, or (stack) a copy in
+  // shared memory made at the start of each layer, followed by the next
+  // layer's (read by the thread that issues its early copies)
+  DecodeLayer* const s_ly = reinterpret_cast<DecodeLayer*>(sm + a.plan.off_misc + 256);
+  // (stack) the block's rows of the layer's input, for the residual: warp 0's
+  // lanes write and read their own entries
+  float* const s_hres = reinterpret_cast<float*>(sm + a.plan.off_misc + 256 + 2 * sizeof(DecodeLayer));
+  auto ly = [&]() -> const DecodeLayer& {
+    if constexpr (kStack)
+      return *s_ly;
+    else
+      return a.ly;
+  };
+  // layers l and l + 1 (when there is one) into s_ly[0], s_ly[1]: threads
+  // 0..17; read after the next block barrier
+  auto copy_layer = [&](int l) {
+    constexpr int kWords = (int)(sizeof(DecodeLayer) / 8);
+    if (tid < (l + 1 < nlayers ? 2 : 1) * kWords)
+      reinterpret_cast<unsigned long long*>(s_ly)[tid] = reinterpret_cast<const unsigned long long*>(layers + l)[tid];
+  };
+  // the thread that issues the next layer's early copies: one with no SwiGLU
+  // rows (at most 9 experts x 32 rows per block) that sums a down row only in
+  // blocks with more than 30 of them
+  constexpr int kPrefetchTid = kBlock - 32;
   const size_t gu_slot = a.plan.gu_slot, dn_slot = a.plan.dn_slot;
   const int part_stride = a.plan.part_stride;
   // mbarriers: [0] router rows, [1 + p] gate/up of expert p, [1 + NE + p] down
-  // of expert p (expert p = 0 is the shared expert when present), then h
+  // of expert p (expert p = 0 is the shared expert when present), then h.
+  // Each completes one phase per copy.
   const int bar_h = 1 + 2 * NE, nbar = bar_h + 1;
+  auto parity = [&](int i) -> uint32_t {
+    if constexpr (kStack)
+      return (*(volatile uint32_t*)&s_mask[8] >> i) & 1u;
+    else
+      return 0u;
+  };
+  float hres = 0.f;    // h[j0 + tid] of the layer's input (threads < nj; one layer)
   float* const hbuf = reinterpret_cast<float*>(G + a.plan.off_hbuf);
 
   // ---- prologue.
@@ -224,40 +286,45 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
   // activations (polled words).
   // Barrier set-up, visible to every thread and to the copy engine before the
   // first copy is issued:
-  if (tid == 0) {
-    STAMP(0);
-    for (int i = 0; i < nbar; ++i) mbar_init(&bar[i], 1);
-    fence_mbar_init();
-    fence_proxy_async();
-    s_mask[0] = 0u;
-    s_mask[1] = 0u;
-    s_mask[4] = 0u;  // counters this block has bumped (bit 0 logits, bit 1 activations)
+  if (l == 0) {
+    if (tid == 0) {
+      STAMP(0);
+      for (int i = 0; i < nbar; ++i) mbar_init(&bar[i], 1);
+      fence_mbar_init();
+      fence_proxy_async();
+      s_mask[0] = 0u;
+      s_mask[1] = 0u;
+      s_mask[4] = 0u;  // counters this block has bumped (bit 0 logits, bit 1 activations)
+      s_mask[6] = 0u;
+      s_mask[8] = 0u;
+    }
+    if constexpr (kStack) copy_layer(0);
+    __syncthreads();
   }
-  __syncthreads();
   // copies of the prologue: bit 0 router rows, bit 1 shared gate/up rows, bit 2
   // shared down rows.  Without PDL h goes first, then the rest in the order they
   // are needed.  With PDL the shared expert's rows (needed last) go out before
   // the dependency wait, and h and the router rows (needed first) right after
   // it, so that they do not queue behind the shared rows.
-  auto issue = [&](uint32_t which) {
+  auto issue = [&](uint32_t which, const DecodeLayer& y) {
     uint32_t issued = 0u;
     if ((which & 1u) && nrr > 0) {
       mbar_expect_tx(&bar[0], (uint32_t)nrr * H * 2);
       uint8_t* rt = G + a.plan.off_rt;
-      if (ne > 0) bulk_g2s(rt, a.router + (size_t)e0 * H, (uint32_t)ne * H * 2, &bar[0]);
-      if (nrr > ne) bulk_g2s(rt + (size_t)ne * H * 2, a.gate, (uint32_t)H * 2, &bar[0]);
+      if (ne > 0) bulk_g2s(rt, y.router + (size_t)e0 * H, (uint32_t)ne * H * 2, &bar[0]);
+      if (nrr > ne) bulk_g2s(rt + (size_t)ne * H * 2, y.gate, (uint32_t)H * 2, &bar[0]);
       issued |= 1u;
     }
     if ((which & 2u) && hs && nr > 0) {
       const uint32_t bytes = (uint32_t)nr * s_gu_pair;
       mbar_expect_tx(&bar[1], bytes);
-      bulk_g2s(G + a.plan.off_sgu, a.shared + (size_t)r0 * s_gu_pair, bytes, &bar[1]);
+      bulk_g2s(G + a.plan.off_sgu, y.shared + (size_t)r0 * s_gu_pair, bytes, &bar[1]);
       issued |= 2u;
     }
     if ((which & 4u) && hs && nj > 0) {
       const uint32_t bytes = (uint32_t)nj * s_d_row;
       mbar_expect_tx(&bar[1 + NE], bytes);
-      bulk_g2s(D, a.shared + s_d_off + (size_t)j0 * s_d_row, bytes, &bar[1 + NE]);
+      bulk_g2s(D, y.shared + s_d_off + (size_t)j0 * s_d_row, bytes, &bar[1 + NE]);
       issued |= 2u << NE;
     }
     return issued;
@@ -268,39 +335,101 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     return 1u << bar_h;
   };
   constexpr uint32_t kEarly = 6u;
-  if (tid == 0) s_mask[0] = kPDL ? issue(kEarly) : (issue_h() | issue(7u));
-  if (kPDL) {
-    pdl_launch_dependents();
-    pdl_wait_prior();
-    if (tid == 0) s_mask[0] |= issue_h() | issue(7u & ~kEarly);
+  if (l == 0) {
+    if (tid == 0) s_mask[0] = kPDL ? issue(kEarly, ly()) : (issue_h() | issue(7u, ly()));
+    if (kPDL) {
+      pdl_launch_dependents();
+      pdl_wait_prior();
+      if (tid == 0) s_mask[0] |= issue_h() | issue(7u & ~kEarly, ly());
+    }
   }
 
-  // one warp waits on mbarrier i (one phase per launch); a give-up is recorded
-  // and acted on at the next block barrier, so that all threads leave together
+  // one warp waits on mbarrier i (its phase of this layer); a give-up is
+  // recorded and acted on at the next block barrier, so that all threads leave
+  // together
   auto warp_wait = [&](int i) -> bool {  // none once the block has failed
-    const bool ok = *(volatile uint32_t*)&s_mask[1] == 0u && mbar_wait(&bar[i], 0);
+    const bool ok = *(volatile uint32_t*)&s_mask[1] == 0u && mbar_wait(&bar[i], parity(i));
     if (!ok && lane == 0) atomicOr(&s_mask[1], 1u);
     return __all_sync(0xffffffffu, ok);
   };
   auto failed = [&]() -> bool { return __syncthreads_or(tid == 0 && s_mask[1] != 0u) != 0; };
 
   // ---- this launch's epoch
-  if (tid == 0) {
-    // every block of every launch adds one, so this launch is number count / P
-    const unsigned long long n = atomicAdd(&a.hdr->launches, 1ull);
-    s_mask[2] = (uint32_t)(n / (unsigned long long)P + 1ull);
-    s_mask[3] = *(volatile uint32_t*)&a.hdr->bar_extra;  // test hook: readers expect a later epoch
+  if (l == 0) {
+    if (tid == 0) {
+      // every block adds one now and, after the last layer, one for every
+      // further layer, so this launch's first layer is number count / P
+      const unsigned long long n = atomicAdd(&a.hdr->launches, 1ull);
+      s_mask[2] = (uint32_t)(n / (unsigned long long)P + 1ull);
+      s_mask[3] = *(volatile uint32_t*)&a.hdr->bar_extra;  // test hook: readers expect a later epoch
+      // no block of this launch adds to the output-row counter before every
+      // block has published its layer-0 activations, which each does after
+      // this read (acquire: the read is not reordered after them)
+      if constexpr (kStack) *s_hbase = ld_acquire_u64(&a.hdr->published_h);
+    }
+    if (__syncthreads_or(tid == 0 && *(volatile uint32_t*)&a.hdr->abort)) goto cleanup;
   }
-  if (__syncthreads_or(tid == 0 && *(volatile uint32_t*)&a.hdr->abort)) goto cleanup;
-  warp_wait(bar_h);
-  if (tid == 0) STAMP(1);
   {
-    float4 hv0 = 4 * tid < H ? reinterpret_cast<const float4*>(hbuf)[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 hv1 =
-        4 * (tid + kBlock) < H ? reinterpret_cast<const float4*>(hbuf)[tid + kBlock] : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float hres = tid < nj ? hbuf[j0 + tid] : 0.f;
-    const uint32_t epoch = s_mask[2];           // written with every published word
-    const uint32_t expect = epoch + s_mask[3];  // awaited by every reader
+    const uint32_t epoch = s_mask[2] + (uint32_t)l;  // written with every published word
+    const uint32_t expect = epoch + s_mask[3];        // awaited by every reader
+    float4 hv0, hv1;
+    if (!kStack || l == 0) {
+      warp_wait(bar_h);
+      if (tid == 0) STAMP(1);
+      hv0 = 4 * tid < H ? reinterpret_cast<const float4*>(hbuf)[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
+      hv1 = 4 * (tid + kBlock) < H ? reinterpret_cast<const float4*>(hbuf)[tid + kBlock] : make_float4(0.f, 0.f, 0.f, 0.f);
+      hres = tid < nj ? hbuf[j0 + tid] : 0.f;
+      if constexpr (kStack) {
+        if (tid < nj) s_hres[tid] = hres;
+      }
+    } else {
+      // ---- input: the previous layer's output rows, published by every
+      // block (this block's own rows are already in s_hres).  One
+      // thread waits on the counter; every thread then loads its 8 words and
+      // polls the late ones together.
+      copy_layer(l);
+      if (tid == 0) {
+        s_mask[8] ^= s_mask[0];  // each barrier the previous layer used has completed one phase
+        s_mask[0] = s_mask[6];   // copies for this layer issued during the previous one
+        s_mask[6] = 0u;
+        s_mask[4] = 0u;
+        const bool ok = wait_count(a.hdr, &a.hdr->published_h, *s_hbase + (unsigned long long)P * (l + s_mask[3]));
+        s_mask[7] = ok ? 0u : 1u;
+      }
+      if (__syncthreads_or(tid == 0 && s_mask[7] != 0u)) goto cleanup;
+      const uint32_t want = expect - 1u;
+      unsigned long long hw[8];
+      bool late = false;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int j = 4 * (tid + kBlock * (k >> 2)) + (k & 3);
+        hw[k] = j < H ? ld_pub(pub_h + h_slot(j)) : ((unsigned long long)want << 32);  // past H: zero, ready
+        late |= !pub_ready(hw[k], want);
+      }
+      if (late) {
+        const unsigned long long t0 = globaltimer();
+        int spins = 0;
+        while (late) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (!pub_ready(hw[k], want)) hw[k] = ld_pub(pub_h + h_slot(4 * (tid + kBlock * (k >> 2)) + (k & 3)));
+          late = false;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) late |= !pub_ready(hw[k], want);
+          if (late && (++spins & 63) == 0 &&
+              (*(volatile uint32_t*)&a.hdr->abort || globaltimer() - t0 > kTimeoutNs)) {
+            if (globaltimer() - t0 > kTimeoutNs) {
+              atomicOr(&a.hdr->status, ST_TIMEOUT);
+              atomicExch(&a.hdr->abort, 1u);
+            }
+            atomicOr(&s_mask[1], 1u);  // acted on at the block barrier after the router rows
+            break;
+          }
+        }
+      }
+      hv0 = make_float4(pub_value(hw[0]), pub_value(hw[1]), pub_value(hw[2]), pub_value(hw[3]));
+      hv1 = make_float4(pub_value(hw[4]), pub_value(hw[5]), pub_value(hw[6]), pub_value(hw[7]));
+    }
 
     // ---- x = h * gamma; sum of h^2; limbs of x.  Thread t holds values
     // 4t .. 4t+3 and 4(t+512) .. 4(t+512)+3, so warp w holds groups 2w, 2w+1
@@ -319,8 +448,8 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         const int i0 = 4 * (tid + kBlock * k);
         float4& x = xs[k];
         ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, ss))));
-        if (a.gamma && i0 < H) {
-          const uint2 gw = *reinterpret_cast<const uint2*>(a.gamma + i0);
+        if (ly().gamma && i0 < H) {
+          const uint2 gw = *reinterpret_cast<const uint2*>(ly().gamma + i0);
           x.x *= bf16lo(gw.x); x.y *= bf16hi(gw.x); x.z *= bf16lo(gw.y); x.w *= bf16hi(gw.y);
         }
         st[k] = i0 < H;
@@ -413,7 +542,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         for (int w = 0; w < kWarps; ++w) v += rpart[lane * kWarps + w];
         v *= rs;
         const int e = lane < ne ? e0 + lane : E;  // the shared-gate logit is row E
-        if (e < E && a.offset) v += a.offset[e];
+        if (e < E && ly().offset) v += ly().offset[e];
         st_pub(a.pub_logits + e, v, epoch);
       }
       __syncwarp();
@@ -428,7 +557,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     auto issue_routed = [&](int k0, int k1) {
       uint32_t issued = s_mask[0];
       for (int k = k0; k < k1; ++k) {
-        const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
+        const uint8_t* blob = ly().experts + (size_t)s_idx[k] * ly().stride;
         if (nr > 0) {
           const uint32_t bytes = (uint32_t)nr * r_gu_pair;
           mbar_expect_tx(&bar[1 + hs + k], bytes);
@@ -518,8 +647,8 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
             if (c == 0) {
               if (!ok || nonfinite_x) atomicOr(&a.hdr->status, ST_NONFINITE);
               for (int k = 0; k < K; ++k) {
-                if (a.idx_out) a.idx_out[k] = s_idx[k];
-                if (a.w_out) a.w_out[k] = s_coef[hs + k];
+                if (ly().idx_out) ly().idx_out[k] = s_idx[k];
+                if (ly().w_out) ly().w_out[k] = s_coef[hs + k];
               }
             }
           }
@@ -555,7 +684,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         // (only if routing succeeded: s_idx is written by top-K; this thread
         // raised the failure flag itself when it did not)
         if (wid == 0 && lane == 0 && nj > 0 && *(volatile uint32_t*)&s_mask[1] == 0u) {
-          const uint8_t* blob = a.experts + (size_t)s_idx[k] * a.stride;
+          const uint8_t* blob = ly().experts + (size_t)s_idx[k] * ly().stride;
           const uint32_t bytes = (uint32_t)nj * r_d_row;
           mbar_expect_tx(&bar[1 + NE + hs + k], bytes);
           bulk_g2s(D + (size_t)(hs + k) * dn_slot, blob + r_d_off + (size_t)j0 * r_d_row, bytes, &bar[1 + NE + hs + k]);
@@ -568,6 +697,15 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
     // coefficient, published for every block
     if (failed()) goto cleanup;
     if (tid == 0) STAMP(16);
+    if constexpr (kStack) {
+      // the routed gate/up slices are dead: the next layer's router rows and
+      // shared gate/up rows go to the gate/up area now (the down partials lie
+      // past both)
+      if (tid == kPrefetchTid && l + 1 < nlayers) {
+        fence_proxy_async();  // the generic-proxy reads of the slices are complete (block barrier)
+        s_mask[6] = issue(3u, s_ly[1]);
+      }
+    }
     for (int t = tid; t < NE * nr; t += kBlock) {
       const int p = t / nr, i = t - p * nr;
       const float* pb = part + (size_t)p * part_stride;
@@ -679,7 +817,7 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         const int p = q / ngi, g = q - p * ngi;
         // lanes of one warp may belong to different experts: each thread waits
         // for its own expert's rows (no warp collective in this section)
-        if (!mbar_wait(&bar[1 + NE + p], 0)) atomicOr(&s_mask[1], 1u);
+        if (!mbar_wait(&bar[1 + NE + p], parity(1 + NE + p))) atomicOr(&s_mask[1], 1u);
         Limbs L;
         load_limbs(AL + (size_t)p * ngi * kLimbBytes, ngi, g, L);
         const float2 es = AE[(size_t)p * ngi + g];
@@ -703,6 +841,13 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
       }
       if (failed()) goto cleanup;
       if (tid == 0) STAMP(21);
+      if constexpr (kStack) {
+        // the down slices are dead: the next layer's shared down rows go to slot 0
+        if (tid == kPrefetchTid && l + 1 < nlayers) {
+          fence_proxy_async();
+          s_mask[6] |= issue(4u, s_ly[1]);
+        }
+      }
       // row r: 16 threads sum every 16th partial, then a butterfly over the 16
       {
         const int r = tid >> 4, sub = tid & 15;
@@ -714,24 +859,71 @@ __global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const DecodeArgs a
         if (sub == 0 && r < nj) ysm[r] = v;
       }
       __syncthreads();
-      if (tid < nj) a.h[j0 + tid] = hres + ysm[tid];
+      // ---- output rows (warp 0's lanes: nj <= 32): h += y after the last
+      // layer, else published as the next layer's input
+      if (wid == 0) {
+        if (lane < nj) {
+          const float hn = (kStack ? s_hres[lane] : hres) + ysm[lane];
+          if (l + 1 == nlayers)
+            a.h[j0 + lane] = hn;
+          else
+            st_pub(pub_h + h_slot(j0 + lane), hn, epoch);
+          if constexpr (kStack) s_hres[lane] = hn;
+        }
+        if (kStack && l + 1 < nlayers) {
+          __syncwarp();
+          if (lane == 0) red_relaxed_add_u64(&a.hdr->published_h, 1ull);
+        }
+      }
       if (tid == 0) STAMP(22);
     }
   }
-  return;
+  if constexpr (kStack) {
+    // the launch's further layers, counted once its last layer is done
+    if (tid == 0 && l + 1 == nlayers && nlayers > 1)
+      red_relaxed_add_u64(&a.hdr->launches, (unsigned long long)(nlayers - 1));
+  }
+  return true;
 
 cleanup:
   // leave only after this block's own copies in flight have landed, and with
-  // every counter advanced by this block as in a complete launch
+  // the epoch counters advanced by this block as in a complete launch (one per
+  // layer: those of the layer that failed still owed, and all of the later
+  // layers').  The output-row counter needs nothing: a stack launch reads it
+  // afresh.
   __syncthreads();
   if (tid == 0) {
-    if (!(s_mask[4] & 1u)) red_relaxed_add_u64(&a.hdr->published_logits, 1ull);
-    if (!(s_mask[4] & 2u)) red_relaxed_add_u64(&a.hdr->published_act, 1ull);
-    const uint32_t issued = s_mask[0];
-    for (int i = 0; i < nbar; ++i)
-      if (issued >> i & 1u) mbar_wait(&bar[i], 0);
+    const unsigned long long later = (unsigned long long)(nlayers - 1 - l);
+    const uint32_t bumped = s_mask[4];
+    const unsigned long long owed_lg = (bumped & 1u ? 0ull : 1ull) + later;
+    const unsigned long long owed_act = (bumped & 2u ? 0ull : 1ull) + later;
+    if (owed_lg) red_relaxed_add_u64(&a.hdr->published_logits, owed_lg);
+    if (owed_act) red_relaxed_add_u64(&a.hdr->published_act, owed_act);
+    if (nlayers > 1) red_relaxed_add_u64(&a.hdr->launches, (unsigned long long)(nlayers - 1));
+    // copies of this layer, and (stack) those already issued for the next one,
+    // which complete the following phase of their barrier
+    const uint32_t issued = s_mask[0], next = s_mask[6], ph = kStack ? s_mask[8] : 0u;
+    for (int i = 0; i < nbar; ++i) {
+      if (issued >> i & 1u) mbar_wait(&bar[i], (ph >> i) & 1u);
+      if (next >> i & 1u) mbar_wait(&bar[i], ((ph ^ issued) >> i) & 1u);
+    }
   }
   __syncthreads();
+  return false;
+}
+
+template <bool kPDL, int kRB, int kSB>
+__global__ void __launch_bounds__(kBlock, 1) decode_b1_kernel(const __grid_constant__ DecodeArgs a) {
+  decode_body<kPDL, kRB, kSB, false>(a, nullptr, 1, nullptr, 0);
+}
+
+template <bool kPDL, int kRB, int kSB>
+__global__ void __launch_bounds__(kBlock, 1) decode_stack_kernel(const __grid_constant__ StackArgs a) {
+  // one body for every layer: its code stays in the instruction cache (a copy
+  // of the body specialised for layer 0 cost ~40 us a launch in instruction
+  // fetches)
+  for (int l = 0; l < a.L; ++l)
+    if (!decode_body<kPDL, kRB, kSB, true>(a.d, a.layers, a.L, a.pub_h, l)) return;
 }
 
 #ifdef MOE_TIMELINE
@@ -782,10 +974,13 @@ bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, i
   };
   p.off_sgu = sub(has_shared ? (size_t)p.rows_gu * fs.gu_pair : 0);
   p.off_rt = sub((size_t)p.rows_r * H * 2);
-  p.off_hbuf = sub((size_t)H * 4);  // h, one bulk copy
-  // after the gate/up phase: the down partials
+  p.off_hbuf = sub((size_t)H * 4);  // h, one bulk copy (first layer)
+  // after the gate/up phase: the down partials, past the shared slice and the
+  // router rows (where a stack launch copies the next layer's while the down
+  // partials are in use); h is dead by then
+  p.off_pdn = p.off_hbuf;
   const size_t post = ((size_t)p.rows_d * NE * fr.ng_i * 4 + 127) / 128 * 128;
-  p.off_g = take(std::max(std::max(pre, (size_t)K * p.gu_slot), post));
+  p.off_g = take(std::max(std::max(pre, (size_t)K * p.gu_slot), p.off_pdn + post));
   // limbs: of x first (read into registers), later of every expert's activation
   const size_t ngroups = std::max((size_t)NE * fr.ng_i, (size_t)fr.ng_h);
   p.off_al = take(ngroups * kLimbBytes);
@@ -795,7 +990,8 @@ bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, i
   p.off_rpart = take((size_t)p.rows_r * kWarps * 4);
   p.off_y = take((size_t)p.rows_d * 4);
   p.off_bar = take((size_t)(1 + 2 * NE + 1) * 8);
-  p.off_misc = take(256);
+  // scalars, then (stack) the layer's pointers and the block's input rows
+  p.off_misc = take(256 + 2 * sizeof(DecodeLayer) + 32 * 4);
   p.total = o + 128;  // slack for rounding the dynamic base up to 128 bytes
   if (p.total > (size_t)optin) return false;
   *out = p;
@@ -811,24 +1007,27 @@ bool decode_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_
 }
 
 namespace {
-template <bool kPDL>
-using DecodeKernel = void (*)(DecodeArgs);
 // the instantiation for (PDL, routed bits, shared bits); without a shared
 // expert the shared width is the routed one
-template <bool kPDL>
-DecodeKernel<kPDL> decode_kernel_for(int bits, int shared_bits) {
-  if (bits == 4) return shared_bits == 4 ? decode_b1_kernel<kPDL, 4, 4> : decode_b1_kernel<kPDL, 4, 2>;
-  return shared_bits == 4 ? decode_b1_kernel<kPDL, 2, 4> : decode_b1_kernel<kPDL, 2, 2>;
+template <bool kPDL, bool kStack>
+auto decode_kernel_for(int bits, int shared_bits) {
+  if constexpr (kStack) {
+    if (bits == 4) return shared_bits == 4 ? decode_stack_kernel<kPDL, 4, 4> : decode_stack_kernel<kPDL, 4, 2>;
+    return shared_bits == 4 ? decode_stack_kernel<kPDL, 2, 4> : decode_stack_kernel<kPDL, 2, 2>;
+  } else {
+    if (bits == 4) return shared_bits == 4 ? decode_b1_kernel<kPDL, 4, 4> : decode_b1_kernel<kPDL, 4, 2>;
+    return shared_bits == 4 ? decode_b1_kernel<kPDL, 2, 4> : decode_b1_kernel<kPDL, 2, 2>;
+  }
 }
-}  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s) {
+template <bool kStack, class Args>
+cudaError_t launch_any(const Args& args, const DecodeArgs& a, bool pdl, cudaStream_t s) {
   static std::atomic<int> configured[2][4][kMaxDevices];  // per PDL variant, code widths and device
   const int bytes = (int)a.plan.total;
   const int sb = a.has_shared ? a.shared_bits : a.bits;
   const int v = (a.bits == 4 ? 0 : 2) + (sb == 4 ? 0 : 1);
-  const DecodeKernel<true> kp = decode_kernel_for<true>(a.bits, sb);
-  const DecodeKernel<false> kn = decode_kernel_for<false>(a.bits, sb);
+  const auto kp = decode_kernel_for<true, kStack>(a.bits, sb);
+  const auto kn = decode_kernel_for<false, kStack>(a.bits, sb);
   const cudaError_t e = pdl ? ensure_dynamic_smem(kp, bytes, configured[1][v])
                             : ensure_dynamic_smem(kn, bytes, configured[0][v]);
   if (e != cudaSuccess) return e;
@@ -849,7 +1048,15 @@ cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return pdl ? cudaLaunchKernelEx(&cfg, kp, a) : cudaLaunchKernelEx(&cfg, kn, a);
+  return pdl ? cudaLaunchKernelEx(&cfg, kp, args) : cudaLaunchKernelEx(&cfg, kn, args);
+}
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s) { return launch_any<false>(a, a, pdl, s); }
+
+cudaError_t launch_decode_stack(const StackArgs& a, bool pdl, cudaStream_t s) {
+  if (a.L < 1 || a.L > kMaxStackLayers) return cudaErrorInvalidValue;
+  return launch_any<true>(a, a.d, pdl, s);
 }
 
 }  // namespace moe

@@ -69,15 +69,20 @@ struct WsHeader {
   uint32_t rsv[2];
   uint32_t bar_extra;  // test hook: added to the epoch every cross-block wait expects (0 in normal use)
   uint32_t rsv2[3];
-  // blocks of the single-token kernel that ever started: each launch adds its
-  // grid size, so a block finds its launch's epoch as count / grid + 1
+  // layers started by the blocks of the single-token kernels: every block adds
+  // one per layer (a launch of L layers adds L per block), so the first layer
+  // of a launch finds its epoch as count / grid + 1 and layer l of the launch
+  // has that epoch + l
   unsigned long long launches;
-  // blocks that finished publishing their logits / activations (each launch
-  // adds its grid size to each): a hint that lets one thread per block wait
-  // on a single word before the epoch-checked reads
+  // blocks that finished publishing their logits / activations (each layer
+  // adds its grid size to each): a hint that lets one thread per block wait on
+  // a single word before the epoch-checked reads
   unsigned long long published_logits;
   unsigned long long published_act;
-  uint32_t rsv3[2];
+  // blocks of stack launches that published a layer's output rows for the
+  // next layer (each such layer adds its grid size); a stack launch reads it
+  // at its start and waits for its own layers' increments above that value
+  unsigned long long published_h;
 };
 static_assert(sizeof(WsHeader) == 64, "header size");
 constexpr size_t kHeaderErrorBytes = 32;
@@ -138,6 +143,11 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {

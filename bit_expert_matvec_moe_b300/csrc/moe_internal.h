@@ -123,28 +123,47 @@ struct DecodePlan {
   size_t off_dn;    // down slices, slot p at off_dn + p * dn_slot
   size_t off_g;     // gate/up area (before routing: shared slice, router rows)
   size_t off_sgu, off_rt, off_hbuf;  // relative to off_g, before routing
+  size_t off_pdn;   // relative to off_g: down partials, after the gate/up phase
   size_t off_al, off_ae;   // limbs of x, later of every expert's activation
   size_t off_part, off_rpart, off_y, off_bar, off_misc;
   size_t total;
 };
 
-struct DecodeArgs {
-  int H, I, E, K, bits, shared_bits, has_shared, has_gate;
-  float eps;
+// The weights and per-layer outputs of one layer (9 words: the stack kernel
+// copies them into shared memory word by word).
+struct DecodeLayer {
   const uint8_t* experts;
   size_t stride;
   const uint8_t* shared;
   const uint16_t* router;
   const uint16_t* gamma;
   const uint16_t* gate;
-  float* h;
   const float* offset;
   int32_t* idx_out;
   float* w_out;
+};
+static_assert(sizeof(DecodeLayer) == 72, "DecodeLayer is copied as 9 words");
+
+struct DecodeArgs {
+  int H, I, E, K, bits, shared_bits, has_shared, has_gate;
+  float eps;
+  float* h;
   WsHeader* hdr;
   unsigned long long* pub_logits;  // [E + 1] published words
   unsigned long long* pub_act;     // [(K + 1), I] published words (weighted activations)
   DecodePlan plan;
+  DecodeLayer ly;                  // the layer (single-layer kernel)
+};
+
+// Layers of one token in one launch of the single-token kernel: layer l's
+// output is layer l + 1's input.  Every layer has the shape and code widths
+// of d; d.ly is unused.
+constexpr int kMaxStackLayers = 64;
+struct StackArgs {
+  DecodeArgs d;
+  unsigned long long* pub_h;  // [H rounded up to 128] published words: a layer's output rows
+  int L;
+  DecodeLayer layers[kMaxStackLayers];
 };
 
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t s);
@@ -165,6 +184,7 @@ bool decode_plan(int H, int I, int E, int K, int bits, int shared_bits, int has_
 bool decode_plan_for(int nsm, int optin, int H, int I, int E, int K, int bits, int shared_bits, int has_shared,
                      int has_gate, DecodePlan* out);
 cudaError_t launch_decode(const DecodeArgs& a, bool pdl, cudaStream_t s);
+cudaError_t launch_decode_stack(const StackArgs& a, bool pdl, cudaStream_t s);
 
 // Launches of the multi-kernel path.  Inside a PdlScope that is on, kernels go
 // out with programmatic stream serialisation: each may be scheduled while its

@@ -136,16 +136,16 @@ moe_status moe_layer_decode_noalloc(const moe_layer* layer, float* h, const floa
   f.has_shared = has_shared;
   f.has_gate = has_gate;
   f.eps = d.rms_eps;
-  f.experts = static_cast<const uint8_t*>(layer->experts);
-  f.stride = layer->expert_stride;
-  f.shared = static_cast<const uint8_t*>(layer->shared);
-  f.router = layer->router;
-  f.gamma = layer->rms_gamma;
-  f.gate = layer->shared_gate;
+  f.ly.experts = static_cast<const uint8_t*>(layer->experts);
+  f.ly.stride = layer->expert_stride;
+  f.ly.shared = static_cast<const uint8_t*>(layer->shared);
+  f.ly.router = layer->router;
+  f.ly.gamma = layer->rms_gamma;
+  f.ly.gate = layer->shared_gate;
   f.h = h;
-  f.offset = logit_offset;
-  f.idx_out = idx_out;
-  f.w_out = w_out;
+  f.ly.offset = logit_offset;
+  f.ly.idx_out = idx_out;
+  f.ly.w_out = w_out;
   f.hdr = reinterpret_cast<WsHeader*>(base);
   f.pub_logits = reinterpret_cast<unsigned long long*>(base + off_logits);
   f.pub_act = reinterpret_cast<unsigned long long*>(base + off_act);

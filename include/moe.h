@@ -204,6 +204,35 @@ moe_status moe_layer_decode(const moe_layer* layer, float* h, int32_t B,
                             void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * One token through n_layers layers in order, in place on h (fp32 [hidden],
+ * device): layer l applies moe_layer_decode's step (B = 1) to the output of
+ * layer l - 1, so that on return h holds the last layer's output.  This is the
+ * per-token layer loop of the pages' engine ("Techniques de rupture" item 3:
+ * expert forward, then combine + norm, then the next layer), with the
+ * per-layer submission gap that the Autoresearch page's "Optimisations
+ * efficaces" removes by pre-encoding taken out by construction: the layers run
+ * in one launch of the single-token kernel (up to 64 layers a launch; longer
+ * stacks take several launches), each layer's router rows and shared-expert
+ * rows copied while the previous layer finishes.
+ *   layers        host array of n_layers layers (1 <= n_layers); every layer
+ *                 has the same moe_dims and shared_bits; the layers' device
+ *                 buffers are read only.
+ *   logit_offset  fp32 [n_layers, n_experts] (layer l's row added to its
+ *                 router logits) or NULL.
+ *   idx_out       int32 [n_layers, K] and w_out fp32 [n_layers, K]: layer l's
+ *                 routing, or NULL.
+ * Results are those of n_layers moe_layer_decode calls (B = 1) on the same
+ * workspace, bit for bit.  Shapes outside the single-token kernel (see
+ * moe_layer_decode), or dims with MOE_NO_FUSED, run as those calls.
+ * MOE_ERR_INVALID_ARG for mismatched dims, null or misaligned pointers, a
+ * workspace smaller than moe_workspace_bytes(dims, 1); device-side errors are
+ * recorded in the workspace status word as for moe_layer_decode.
+ */
+moe_status moe_stack_decode(const moe_layer* layers, int32_t n_layers, float* h,
+                            const float* logit_offset, int32_t* idx_out, float* w_out,
+                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Synchronise `stream`, read the workspace status word, clear it and return
  * it (MOE_OK when no device-side error was recorded).  After a device-side
  * error the kernels of later calls return early until the status is cleared.

@@ -3,7 +3,8 @@
 // shapes the tests and the bench use, and for random shapes inside the kernel's
 // limits, every plan that is accepted must have: regions 128-byte aligned,
 // disjoint and inside the total; the gate/up area holding the pre-routing
-// pieces, the routed slices and the post-gate/up pieces; every block's rows and
+// pieces, the routed slices and the post-gate/up pieces (the down partials
+// clear of the next layer's shared and router rows); every block's rows and
 // copies inside their slots; and the lane and thread mappings covering every
 // row.  Prints "ok <accepted> <rejected>" and exits 0, or names the first
 // violation and exits 1.
@@ -47,7 +48,7 @@ bool check(int nsm, int optin, int H, int I, int E, int K, int bits, int sbits, 
       {"router partials", p.off_rpart, p.off_rpart + (size_t)p.rows_r * moe::kWarps * 4},
       {"down sums", p.off_y, p.off_y + (size_t)p.rows_d * 4},
       {"mbarriers", p.off_bar, p.off_bar + (size_t)(1 + 2 * NE + 1) * 8},
-      {"misc", p.off_misc, p.off_misc + 192}};
+      {"misc", p.off_misc, p.off_misc + 256 + 2 * sizeof(moe::DecodeLayer) + 32 * 4}};
   for (size_t i = 0; i < rs.size(); ++i) {
     if (rs[i].at % 128) return fail(rs[i].name);
     if (rs[i].end + 128 > p.total) return fail("region past the total");
@@ -58,7 +59,12 @@ bool check(int nsm, int optin, int H, int I, int E, int K, int bits, int sbits, 
   if (pre_end > gsz) return fail("pre-routing pieces outside the gate/up area");
   if ((size_t)K * p.gu_slot > gsz) return fail("routed slices outside the gate/up area");
   const size_t pdn = (size_t)p.rows_d * NE * ngi * 4;
-  if (pdn > gsz) return fail("down partials outside the gate/up area");
+  if (p.off_pdn + pdn > gsz) return fail("down partials outside the gate/up area");
+  // a stack launch copies the next layer's shared gate/up rows and router rows
+  // while the down partials are in use
+  const size_t next_end = std::max(p.off_sgu + (hs ? (size_t)p.rows_gu * fs.gu_pair : 0),
+                                   p.off_rt + (size_t)p.rows_r * H * 2);
+  if (p.off_pdn < next_end) return fail("down partials overlap the next layer's rows");
   if (p.off_sgu % 16 || p.off_rt % 16 || p.off_hbuf % 16 || p.gu_slot % 16 || p.dn_slot % 16)
     return fail("copy destination not 16-byte aligned");
   if (p.total > (size_t)optin) return fail("plan larger than the opt-in shared memory");

@@ -99,6 +99,33 @@ def test_host_validation_returns_before_launch(lib):
     assert lib.moe_workspace_init(None, 0, None) == N.MOE_ERR_INVALID_ARG
 
 
+def test_stack_decode_host_validation(lib):
+    """moe_stack_decode refuses on the host (before any CUDA call): no layers,
+    a null layer array, layers whose dims or shared widths differ, a bad layer
+    among good ones, null or misaligned h, a small workspace."""
+    from bit_expert_matvec_moe_b300 import _native as N
+
+    d = dims()
+    good = N.moe_layer(d, 16, 7_077_888, 32, 4, 48, None, None)
+    ws = lib.moe_workspace_bytes(ctypes.byref(d), 1)
+    arr = (N.moe_layer * 2)(good, good)
+    assert lib.moe_stack_decode(arr, 0, 64, None, None, None, 80, ws, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_decode(None, 2, 64, None, None, None, 80, ws, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_decode(arr, 2, None, None, None, None, 80, ws, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_decode(arr, 2, 68, None, None, None, 80, ws, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_decode(arr, 2, 64, None, None, None, 80, ws - 16, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_decode(arr, 2, 64, 66, None, None, 80, ws, None) == N.MOE_ERR_INVALID_ARG  # offsets not 4-aligned
+    other = N.moe_layer(dims(top_k=2), 16, 7_077_888, 32, 4, 48, None, None)
+    assert lib.moe_stack_decode((N.moe_layer * 2)(good, other), 2, 64, None, None, None, 80, ws, None) == \
+        N.MOE_ERR_INVALID_ARG
+    two_bit_shared = N.moe_layer(d, 16, 7_077_888, 32, 2, 48, None, None)
+    assert lib.moe_stack_decode((N.moe_layer * 2)(good, two_bit_shared), 2, 64, None, None, None, 80, ws, None) == \
+        N.MOE_ERR_INVALID_ARG
+    bad = N.moe_layer(d, None, 7_077_888, 32, 4, 48, None, None)
+    assert lib.moe_stack_decode((N.moe_layer * 2)(good, bad), 2, 64, None, None, None, 80, ws, None) == \
+        N.MOE_ERR_INVALID_ARG
+
+
 def test_tensor_core_flag_workspace(lib):
     """MOE_TENSOR_CORES is a valid flag: the workspace grows by the tensor-core
     path's operand buffers (B rows of xn and of the activations, fp16 hi and lo,
