@@ -145,15 +145,17 @@ def kernel_source_sha(files=("moe_decode_b1.cu", "moe_device.cuh", "moe_kernels.
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name):
-    """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"{name}.json")
+def profiled_traffic(name, algorithmic_bytes_per_launch):
+    """dram bytes of one launch of the bench's workload: the committed ncu
+    capture's DRAM bytes per algorithmic byte (taken on a smaller expert pool,
+    whose layers differ only in the router's rows) times the launch's
+    algorithmic bytes, if the capture was taken on the current kernel sources;
+    else None."""
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, "profiles", f"{name}.json")) as f:
             p = json.load(f)
         if p.get("source_sha") == kernel_source_sha():
-            return p.get("dram_bytes_per_launch")
+            return int(round(p["dram_over_algorithmic"] * algorithmic_bytes_per_launch))
     except Exception:  # noqa: BLE001
         pass
     return None
@@ -364,7 +366,7 @@ def run_ours(args, rank, world, local):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4) if achieved else None,
             "algorithmic_bytes_per_launch": alg,
-            "traffic": (profiled_traffic("decode_b1_full_b1") if (B == 1 and bits == 4) else
+            "traffic": (profiled_traffic("decode_b1_full_b1", alg) if (B == 1 and bits == 4) else
                         profiled_tc_traffic(uniq + 1) if (tc and bits == 4) else None),
         },
         "e2e": {"value": round(job_throughput(T, world, e2e), 1), "unit": "tokens/s",
@@ -525,7 +527,9 @@ def run_stack(args, rank, world, local):
             "bound": "hbm", "kernel": "decode_b1_kernel" if args.per_layer else "decode_stack_kernel",
             "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "algorithmic_bytes_per_launch": int(layer_bytes * (T * Lyr // launches)), "traffic": None,
+            "algorithmic_bytes_per_launch": int(layer_bytes * (T * Lyr // launches)),
+            "traffic": profiled_traffic("decode_b1_full_b1" if args.per_layer else "decode_stack_full_b1",
+                                        layer_bytes * (T * Lyr // launches)),
         },
         "e2e": {"value": round(job_throughput(T, world, e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_pin.numel() * 4), "d2h_bytes_per_step": int(y_pin.numel() * 4)},
