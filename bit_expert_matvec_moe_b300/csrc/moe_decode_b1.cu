@@ -513,25 +513,39 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const DecodeLay
     if (nrr > 0) warp_wait(0);
     if (tid == 0) STAMP(3);
     {
+      // four rows at a time, their warp reductions interleaved (the same
+      // butterfly per row as warp_sum, so the sums do not change)
       const uint8_t* rt = G + a.plan.off_rt;
-      for (int ri = 0; ri < nrr; ++ri) {
-        float acc = 0.f;
-        if (4 * tid < H) {
-          const uint2 rw = *reinterpret_cast<const uint2*>(rt + ((size_t)ri * H + 4 * tid) * 2);
-          acc = fmaf(bf16lo(rw.x), hv0.x, acc);
-          acc = fmaf(bf16hi(rw.x), hv0.y, acc);
-          acc = fmaf(bf16lo(rw.y), hv0.z, acc);
-          acc = fmaf(bf16hi(rw.y), hv0.w, acc);
+      for (int rb = 0; rb < nrr; rb += 4) {
+        float acc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int ri = rb + q;
+          acc[q] = 0.f;
+          if (ri < nrr && 4 * tid < H) {
+            const uint2 rw = *reinterpret_cast<const uint2*>(rt + ((size_t)ri * H + 4 * tid) * 2);
+            acc[q] = fmaf(bf16lo(rw.x), hv0.x, acc[q]);
+            acc[q] = fmaf(bf16hi(rw.x), hv0.y, acc[q]);
+            acc[q] = fmaf(bf16lo(rw.y), hv0.z, acc[q]);
+            acc[q] = fmaf(bf16hi(rw.y), hv0.w, acc[q]);
+          }
+          if (ri < nrr && 4 * (tid + kBlock) < H) {
+            const uint2 rw = *reinterpret_cast<const uint2*>(rt + ((size_t)ri * H + 4 * (tid + kBlock)) * 2);
+            acc[q] = fmaf(bf16lo(rw.x), hv1.x, acc[q]);
+            acc[q] = fmaf(bf16hi(rw.x), hv1.y, acc[q]);
+            acc[q] = fmaf(bf16lo(rw.y), hv1.z, acc[q]);
+            acc[q] = fmaf(bf16hi(rw.y), hv1.w, acc[q]);
+          }
         }
-        if (4 * (tid + kBlock) < H) {
-          const uint2 rw = *reinterpret_cast<const uint2*>(rt + ((size_t)ri * H + 4 * (tid + kBlock)) * 2);
-          acc = fmaf(bf16lo(rw.x), hv1.x, acc);
-          acc = fmaf(bf16hi(rw.x), hv1.y, acc);
-          acc = fmaf(bf16lo(rw.y), hv1.z, acc);
-          acc = fmaf(bf16hi(rw.y), hv1.w, acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        if (lane == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (rb + q < nrr) rpart[(rb + q) * kWarps + wid] = acc[q];
         }
-        acc = warp_sum(acc);
-        if (lane == 0) rpart[ri * kWarps + wid] = acc;
       }
     }
     if (failed()) goto cleanup;
