@@ -39,10 +39,10 @@
 // them): hidden <= 4096, inter <= 2048, experts <= 1024, top-K <= 8, and the
 // plan must fit in shared memory.
 //
-// With programmatic dependent launch (kPDL) the shared expert's rows are
-// copied before griddepcontrol.wait, i.e. while the previous kernel on the
-// stream may still run; nothing the caller writes (h, offsets, workspace) is
-// read before that wait.
+// With programmatic dependent launch (kPDL) the router rows are copied before
+// griddepcontrol.wait, i.e. while the previous kernel on the stream may still
+// run; nothing the caller writes (h, offsets, workspace) is read before that
+// wait.
 //
 // decode_stack_kernel runs the layers of one token in one launch, the same
 // phases once per layer.  Layer l's output rows are published like the
@@ -303,9 +303,11 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const DecodeLay
   }
   // copies of the prologue: bit 0 router rows, bit 1 shared gate/up rows, bit 2
   // shared down rows.  Without PDL h goes first, then the rest in the order they
-  // are needed.  With PDL the shared expert's rows (needed last) go out before
-  // the dependency wait, and h and the router rows (needed first) right after
-  // it, so that they do not queue behind the shared rows.
+  // are needed.  With PDL the router rows (needed right after h) go out before
+  // the dependency wait, h and then the shared expert's rows (needed once the
+  // logits are out) right after it: in a block's copy engine nothing queues
+  // ahead of h but the router rows.  (Shared rows before the wait as well put
+  // more ahead of h and crowd the previous launch's tail: slower.)
   auto issue = [&](uint32_t which, const DecodeLayer& y) {
     uint32_t issued = 0u;
     if ((which & 1u) && nrr > 0) {
@@ -334,7 +336,7 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const DecodeLay
     bulk_g2s(hbuf, a.h, (uint32_t)H * 4, &bar[bar_h]);
     return 1u << bar_h;
   };
-  constexpr uint32_t kEarly = 6u;
+  constexpr uint32_t kEarly = 1u;
   if (l == 0) {
     if (tid == 0) s_mask[0] = kPDL ? issue(kEarly, ly()) : (issue_h() | issue(7u, ly()));
     if (kPDL) {
