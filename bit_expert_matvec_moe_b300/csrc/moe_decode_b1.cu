@@ -14,9 +14,10 @@
 // every block reads in full, one relaxed counter tells a reader when every
 // block has published, and late words are polled again after it.
 // Phases of a block:
-//   h -> limbs of h*gamma (the RMS factor r multiplies each gate/up dot
-//        product, so quantisation does not wait for the norm); r from a block sum
+//   h -> h*gamma and a block sum for the RMS factor r
 //   router rows -> published logits
+//   limbs of h*gamma (r multiplies each gate/up dot product instead, so the
+//        limbs do not wait for the norm; quantised once the logits are out)
 //   warps 1..: shared expert gate/up.  Meanwhile warp 0: poll every block's
 //           logits (16 words per lane in flight); top-K (every block, same
 //           result); issue the routed gate/up copies whose slots do not
@@ -433,18 +434,13 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const DecodeLay
       hv1 = make_float4(pub_value(hw[4]), pub_value(hw[5]), pub_value(hw[6]), pub_value(hw[7]));
     }
 
-    // ---- x = h * gamma; sum of h^2; limbs of x.  Thread t holds values
+    // ---- x = h * gamma and the sum of h^2 (the router needs only these; the
+    // limbs of x follow once the logits are out).  Thread t holds values
     // 4t .. 4t+3 and 4(t+512) .. 4(t+512)+3, so warp w holds groups 2w, 2w+1
-    // and 2w+16, 2w+17 (both passes quantised together).
+    // and 2w+16, 2w+17.
     float ss = 0.f;
-    bool finite = true;
     {
       float4 xs[2] = {hv0, hv1};
-      bool st[2];
-      int gs[2];
-      uint8_t* vs[2] = {AL, AL};
-      float2* es[2];
-      const float one[2] = {1.0f, 1.0f};
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int i0 = 4 * (tid + kBlock * k);
@@ -454,18 +450,13 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const DecodeLay
           const uint2 gw = *reinterpret_cast<const uint2*>(ly().gamma + i0);
           x.x *= bf16lo(gw.x); x.y *= bf16hi(gw.x); x.z *= bf16lo(gw.y); x.w *= bf16hi(gw.y);
         }
-        st[k] = i0 < H;
-        gs[k] = st[k] ? i0 / kGroup : 0;
-        es[k] = AE + gs[k];
       }
       hv0 = xs[0];
       hv1 = xs[1];
-      if (4 * 32 * wid < H)  // the warp's first pass has values (whole warps skip)
-        finite = quantize_groups<2>(xs, lane, st, vs, ngh, gs, es, one);
     }
     ss = warp_sum(ss);
     if (lane == 0) s_red[wid] = ss;
-    const int nonfinite_x = __syncthreads_or(!finite);
+    __syncthreads();
     if (tid == 0) STAMP(2);
     float tot = 0.f;
 #pragma unroll
@@ -568,6 +559,27 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const DecodeLay
         s_mask[4] |= 1u;
       }
     }
+    // ---- limbs of x (both passes quantised together), first needed by the
+    // gate/up rows: after the logits are out, off the way to top-K
+    bool finite = true;
+    {
+      float4 xs[2] = {hv0, hv1};
+      bool st[2];
+      int gs[2];
+      uint8_t* vs[2] = {AL, AL};
+      float2* es[2];
+      const float one[2] = {1.0f, 1.0f};
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i0 = 4 * (tid + kBlock * k);
+        st[k] = i0 < H;
+        gs[k] = st[k] ? i0 / kGroup : 0;
+        es[k] = AE + gs[k];
+      }
+      if (4 * 32 * wid < H)  // the warp's first pass has values (whole warps skip)
+        finite = quantize_groups<2>(xs, lane, st, vs, ngh, gs, es, one);
+    }
+    const int nonfinite_x = __syncthreads_or(!finite);
 
     // routed gate/up copies of experts k0 .. k1 - 1 (lane 0 of warp 0)
     auto issue_routed = [&](int k0, int k1) {
