@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -137,11 +138,20 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
-def kernel_source_sha(files=("moe_decode_b1.cu", "moe_device.cuh", "moe_kernels.cu")):
+def _code_only(text: str) -> str:
+    """A source file without its comments and with runs of blank space made one
+    space: a change of wording in a comment leaves a profile valid, any change
+    of code does not."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", " ", text).strip()
+
+
+def kernel_source_sha(files=("moe_decode_b1.cu", "moe_device.cuh", "moe_kernels.cu"), root=None):
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "bit_expert_matvec_moe_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(root or ROOT, "bit_expert_matvec_moe_b300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,9 +8,9 @@
 //   after top-K     gate/up rows of all K routed experts (they fit side by side)
 //   after gate/up k down rows of routed expert k (once its gate/up rows landed)
 // Grid-wide data dependencies go through the workspace: every published word
-// carries the launch's epoch in its upper half (a reader sees either the old
-// word or the new one, never a mix, and polls a word again until its epoch is
-// this launch's).  The logits are polled directly; for the activations, which
+// carries its layer's epoch in its upper half (one epoch per layer, so one per
+// launch of this kernel; a reader sees either the old word or the new one,
+// never a mix, and polls a word again until its epoch is the current layer's).  The logits are polled directly; for the activations, which
 // every block reads in full, one relaxed counter tells a reader when every
 // block has published, and late words are polled again after it.
 // Phases of a block:

@@ -55,9 +55,10 @@ typedef enum {
 #define MOE_HAS_SHARED 1      /* the layer has one always-on shared expert */
 #define MOE_HAS_SHARED_GATE 2 /* the shared expert is scaled by sigmoid(shared_gate . xn) */
 #define MOE_NO_FUSED 4        /* moe_layer_decode: take the multi-kernel path even for B == 1 */
-#define MOE_PDL 8             /* programmatic dependent launch.  moe_layer_decode, B == 1: the
-                                 kernel's weight prefetch overlaps the previous kernel on the stream
-                                 (instead of a cooperative launch; see moe_layer_decode).  B > 1 and
+#define MOE_PDL 8             /* programmatic dependent launch.  moe_layer_decode, B == 1, and
+                                 moe_stack_decode: the kernel's weight prefetch overlaps the previous
+                                 kernel on the stream (instead of a cooperative launch; see
+                                 moe_layer_decode).  B > 1 and
                                  moe_route / moe_expert_forward: each kernel of the multi-kernel path
                                  may be scheduled while its predecessor drains and waits for it on
                                  the device (griddepcontrol.wait) before touching memory. */
