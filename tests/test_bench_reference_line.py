@@ -25,3 +25,26 @@ def test_reference_arm_json_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert "workload" in d["config"]
+
+
+def test_profile_hash_ignores_comments_only():
+    """A committed ncu capture stays valid while the kernel code hashes the
+    same: rewording a comment keeps the hash, a change of code changes it."""
+    import shutil
+    import tempfile
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    files = ("moe_decode_b1.cu", "moe_device.cuh", "moe_kernels.cu")
+    with tempfile.TemporaryDirectory() as tmp:
+        src = os.path.join(ROOT, "bit_expert_matvec_moe_b300", "csrc")
+        dst = os.path.join(tmp, "bit_expert_matvec_moe_b300", "csrc")
+        shutil.copytree(src, dst)
+        base = bench.kernel_source_sha(files, root=tmp)
+        path = os.path.join(dst, "moe_decode_b1.cu")
+        text = open(path, encoding="utf-8").read()
+        open(path, "w", encoding="utf-8").write("// another wording\n/* a block\n   comment */\n" + text + "\n  // tail\n")
+        assert bench.kernel_source_sha(files, root=tmp) == base
+        open(path, "w", encoding="utf-8").write(text.replace("kBlock - 32", "kBlock - 64", 1))
+        assert bench.kernel_source_sha(files, root=tmp) != base
