@@ -54,8 +54,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--experts", type=int, default=512, help="routed experts (smaller pools for profiling runs)")
     p.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch between decode calls")
-    p.add_argument("--per-layer", action="store_true",
-                   help="40-layer stack: one moe_layer_decode call per layer instead of one moe_stack_decode per token")
+    p.add_argument("--stack", action="store_true",
+                   help="40-layer stack: one moe_stack_decode call per token (every layer in one launch) instead of one "
+                        "moe_layer_decode call per layer (PDL-chained launches, the faster form on B300)")
     p.add_argument("--tensor-cores", action="store_true",
                    help="B > 1: expert contractions on the tensor cores (MOE_TENSOR_CORES)")
     return p.parse_args()
@@ -401,9 +402,9 @@ def run_ours(args, rank, world, local):
 # ----------------------------------------------------------------------------- 40-layer stack
 def run_stack(args, rank, world, local):
     """40 full-width 4-bit layers resident in HBM; each token passes all of them
-    (RMSNorm before, residual after each), one moe_stack_decode call per token
-    (every layer in one launch), or with --per-layer one moe_layer_decode call
-    per layer.  Every layer
+    (RMSNorm before, residual after each), one moe_layer_decode call per layer
+    (PDL-chained launches replayed from a graph), or with --stack one
+    moe_stack_decode call per token (every layer in one launch).  Every layer
     has its own copy of the 512-expert pool, shared expert and router (identical
     bytes, distinct addresses: 145 GB of experts), so nothing a token reads is
     left in L2 by the previous token.  Routing follows a reuse trace (token t's
@@ -447,7 +448,7 @@ def run_stack(args, rank, world, local):
 
     def one_step():
         for t in range(T):
-            if args.per_layer:
+            if not args.stack:
                 for l in range(Lyr):
                     M.moe_layer_decode(layers[l], h[t:t + 1], ws, logit_offset=offs[t, l:l + 1],
                                        idx_out=idx[t, l:l + 1], stream=stream)
@@ -503,7 +504,7 @@ def run_stack(args, rank, world, local):
                 e2e_ms.append(e0.elapsed_time(e1))
     e2e = max_over_ranks(float(np.mean(e2e_ms)), world, "cuda")
     layer_bytes = (K + 1) * M.moe_packed_expert_bytes(d, 4) + E * d.hidden * 2
-    launches = T * Lyr if args.per_layer else T * -(-Lyr // 64)
+    launches = T * -(-Lyr // 64) if args.stack else T * Lyr
     tok_s = job_throughput(T, world, ms)
     per_launch_s = ms / 1e3 / (T * Lyr)
     peak, peak_kind = measured_hbm_peak()
@@ -526,7 +527,7 @@ def run_stack(args, rank, world, local):
             "workload": (f"{Lyr}-layer MoE decode stack resident in HBM: full-width 4-bit layers (hidden 4096, {E} experts, "
                          f"top-4 + 1 shared, inter 1024), {T} tokens, top-4 reuse trace p=0.27"),
             "batch": 1, "tokens_per_step": T, "layers": Lyr, "launches_per_step": launches,
-            "entry": "moe_layer_decode per layer" if args.per_layer else "moe_stack_decode per token",
+            "entry": "moe_stack_decode per token" if args.stack else "moe_layer_decode per layer",
             "l2": "no reuse: every layer has its own expert pool, shared expert and router (145 GB of experts)",
             "graph": True, "parallelism": f"replicas x{world}",
         },
@@ -534,11 +535,11 @@ def run_stack(args, rank, world, local):
         "us_per_layer": round(per_launch_s * 1e6, 3),
         "bytes_per_token": int(layer_bytes * Lyr),
         "roofline": {
-            "bound": "hbm", "kernel": "decode_b1_kernel" if args.per_layer else "decode_stack_kernel",
+            "bound": "hbm", "kernel": "decode_stack_kernel" if args.stack else "decode_b1_kernel",
             "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "algorithmic_bytes_per_launch": int(layer_bytes * (T * Lyr // launches)),
-            "traffic": profiled_traffic("decode_b1_full_b1" if args.per_layer else "decode_stack_full_b1",
+            "traffic": profiled_traffic("decode_stack_full_b1" if args.stack else "decode_b1_full_b1",
                                         layer_bytes * (T * Lyr // launches)),
         },
         "e2e": {"value": round(job_throughput(T, world, e2e), 1), "unit": "tokens/s",
