@@ -56,3 +56,23 @@ def test_router_and_pack_argument_checks():
                     torch.zeros((2, 4), dtype=torch.float32), torch.zeros(16, dtype=torch.uint8),
                     logits_out=torch.zeros((2, 15), dtype=torch.float32))
     assert "logits_out: expected at least 32 elements" in str(err.value)
+
+
+@pytest.mark.parametrize("bad, msg", [
+    (dict(layers=[]), "no layers"),
+    (dict(h=torch.zeros((1, 320), dtype=torch.float32)), "h must hold one token"),
+    (dict(h=torch.zeros((2, 256), dtype=torch.float32)), "h must hold one token"),
+    (dict(h=torch.zeros((1, 256), dtype=torch.float16)), "h: expected dtype float32"),
+    (dict(idx_out=torch.zeros((2, 4), dtype=torch.int64)), "idx_out: expected dtype int32"),
+    (dict(w_out=torch.zeros((2, 3), dtype=torch.float32)), "w_out: expected at least 8 elements"),
+    (dict(logit_offset=torch.zeros((1, 16), dtype=torch.float32)), "logit_offset: expected at least 32 elements"),
+])
+def test_stack_decode_argument_checks(bad, msg):
+    """moe_stack_decode: one token ([1, hidden] or [hidden]); per-layer rows of
+    the offsets and outputs for every layer, checked before any device work."""
+    args = dict(layers=[_layer(), _layer()], h=torch.zeros((1, 256), dtype=torch.float32))
+    args.update(bad)
+    layers, h = args.pop("layers"), args.pop("h")
+    with pytest.raises(ValueError) as err:
+        M.moe_stack_decode(layers, h, torch.zeros(16, dtype=torch.uint8), **args)
+    assert msg in str(err.value)
